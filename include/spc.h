@@ -1,0 +1,238 @@
+/*
+ * spc.h -- C ABI of libspc.so: sparse 3-D convolution over voxel coordinate sets.
+ *
+ * The library computes, on one CUDA GPU (sm_103a):
+ *   - the indice map (kernel map) of a submanifold or strided sparse conv,
+ *     built with a GPU open-addressing hash table over int64 cell keys;
+ *   - the output coordinate set of a strided sparse conv (sort + unique);
+ *   - the convolution forward, its input gradient (dinput) and its weight
+ *     gradient (dfilter) as implicit GEMMs over that map.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Coordinates   int32 [n, 4] row-major rows (b, z, y, x), batch index first
+ *                (spconv docs, USAGE.md "Core Concepts Definitions": the
+ *                indices of a sparse conv tensor are stored transposed, one row
+ *                per voxel).  The pointer must be 16-byte aligned.
+ *  Grid          in_shape = (D, H, W) of the (z, y, x) axes, batch in [0, batch).
+ *  Kernel index  k runs in C order over (kz, ky, kx); K = kz*ky*kx (lato_mlx
+ *                sparse/conv.py, "_kernel_offsets": centred offsets in C order
+ *                over (dz, dy, dx), the ordering spconv uses).
+ *  Weights       [K, Cin, Cout] row-major (lato_mlx sparse/conv.py, SubMConv3d
+ *                class docstring, weight layout).
+ *  Features      [rows, C] row-major; dtype given by spc_dtype.
+ *  Indice map    int32 [K, n_out] row-major: imap[k, o] is the input row that
+ *                output row o reads through offset k, or -1 when that cell is
+ *                empty or outside the grid.
+ *  Pointers      every array argument is a DEVICE pointer owned by the caller,
+ *                except those marked "host".  The library keeps no state and
+ *                allocates nothing: scratch memory is a caller-supplied
+ *                workspace of at least the size the matching *_workspace_size
+ *                query returns (256-byte aligned).
+ *  Streams       `stream` is a cudaStream_t (NULL = legacy default stream);
+ *                all device work is enqueued on it and no call synchronises.
+ *  Errors        Argument errors are returned synchronously, before any work
+ *                is enqueued.  Errors that depend on the data (a coordinate out
+ *                of range, a duplicate coordinate, a full hash table, an output
+ *                set larger than its buffer) are written to `status`, a device
+ *                int32 the caller zeroes once: a kernel that finds an error
+ *                stores its spc_status there only if it still holds SPC_OK, so
+ *                the first error sticks.  Read it after synchronising.
+ *                Results written alongside a nonzero status are unspecified.
+ *  Empty input   n = 0 (or an empty output set) is valid and does no work.
+ */
+#ifndef SPC_H
+#define SPC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPC_API __attribute__((visibility("default")))
+#else
+#define SPC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPC_OK = 0,
+    SPC_ERR_INVALID_ARG = 1,   /* bad size, null pointer, misaligned pointer, bad geometry */
+    SPC_ERR_COORD_RANGE = 2,   /* a coordinate lies outside [0,batch) x grid */
+    SPC_ERR_DUPLICATE = 3,     /* two rows hold the same (b, z, y, x) */
+    SPC_ERR_TABLE_FULL = 4,    /* a hash probe exceeded its bound */
+    SPC_ERR_CAPACITY = 5,      /* the strided output set exceeds the caller's buffer */
+    SPC_ERR_UNSUPPORTED = 6,   /* a valid request this build does not implement */
+    SPC_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch, copy) */
+    SPC_ERR_WORKSPACE = 8      /* workspace missing or smaller than required */
+} spc_status;
+
+typedef enum { SPC_F32 = 0, SPC_F16 = 1, SPC_BF16 = 2 } spc_dtype;
+
+/* SPC_PREC_EXACT: fp32 features use full fp32 multiplies; fp16/bf16 features
+ * multiply exactly (their products fit fp32) and accumulate in fp32.
+ * SPC_PREC_TF32: fp32 features are rounded to tf32 before a tensor-core
+ * multiply (accumulation stays fp32); ignored for fp16/bf16. */
+typedef enum { SPC_PREC_EXACT = 0, SPC_PREC_TF32 = 1 } spc_precision;
+
+/* How spc_conv_dgrad reads its map argument. */
+typedef enum {
+    /* map is the transposed map imap_t [K, n_in]: imap_t[k, i] = o for every
+     * pair imap[k, o] = i (what spc_build_indice_map writes for strided maps). */
+    SPC_MAP_TRANSPOSED = 0,
+    /* map is a submanifold map imap [K, n] (n_in == n_out): its transpose is
+     * its offset mirror, imap_t[k, i] = imap[K-1-k, i], so no second map is kept. */
+    SPC_MAP_SUBM_MIRROR = 1
+} spc_map_kind;
+
+/* Convolution geometry per axis (z, y, x). */
+typedef struct {
+    int32_t ksize[3];
+    int32_t stride[3];
+    int32_t pad[3];
+    int32_t dil[3];
+} spc_geom;
+
+/* Human-readable name of a status code (static storage). */
+SPC_API const char* spc_status_string(spc_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SPC_API int32_t spc_version(void);
+
+/* Output grid of a strided (regular) sparse conv, per axis
+ * floor((in + 2 pad - dil (k - 1) - 1) / stride) + 1, or 0 when the window never
+ * fits: the grid a dense conv over the densified input produces (spconv docs,
+ * USAGE.md "Core Concepts Definitions", Sparse Convolution).  Host only. */
+SPC_API spc_status spc_out_shape(const int32_t in_shape[3] /*host*/, const spc_geom* g /*host*/,
+                         int32_t out_shape[3] /*host, out*/);
+
+/* ------------------------------------------------------------------ indice map
+ * spc_build_indice_map -- validate and key the input coordinates, build the
+ * hash table, and probe every (output row, offset) pair.
+ *
+ *  subm != 0 (submanifold conv; spconv USAGE.md "Core Concepts Definitions",
+ *    Submanifold Convolution; lato_mlx sparse/conv.py "build_indice_map"):
+ *    the output set is the input set (out_coords ignored, n_out must equal
+ *    n_in), every ksize must be odd, stride and pad are ignored, and offset k
+ *    reads the cell coords[o] + ((kz - ksz/2) dil_z, (ky - ksy/2) dil_y,
+ *    (kx - ksx/2) dil_x).
+ *  subm == 0 (strided conv): output row o = out_coords[o] (grid
+ *    spc_out_shape(in_shape, g)) reads input cell out*stride - pad + k*dil.
+ *
+ *  coords     [n_in, 4] int32 input coordinates (16-byte aligned).
+ *  out_coords [n_out, 4] int32 output coordinates (strided only, else NULL).
+ *  imap       [K, n_out] int32 out: input row or -1.
+ *  imap_t     [K, n_in] int32 out or NULL: output row or -1, the transpose of
+ *             imap (strided only; must be NULL when subm != 0).
+ *  pair_count [K] int32 out: number of entries != -1 in each row of imap.
+ *  mask       [n_out] uint32 out or NULL: bit k set when imap[k, o] != -1
+ *             (only when K <= 32).
+ *  status     device int32, sticky error word (see above).  Sets
+ *             SPC_ERR_COORD_RANGE, SPC_ERR_DUPLICATE or SPC_ERR_TABLE_FULL.
+ *  ws         workspace of spc_indice_map_workspace_size(n_in) bytes.
+ */
+SPC_API size_t spc_indice_map_workspace_size(int64_t n_in);
+
+SPC_API spc_status spc_build_indice_map(const int32_t* coords, int64_t n_in, int32_t batch,
+                                const int32_t in_shape[3] /*host*/, const spc_geom* g /*host*/,
+                                int32_t subm, const int32_t* out_coords, int64_t n_out,
+                                int32_t* imap, int32_t* imap_t, int32_t* pair_count,
+                                uint32_t* mask, int32_t* status, void* ws, size_t ws_bytes,
+                                void* stream);
+
+/* ------------------------------------------------------ strided output coords
+ * spc_strided_out_coords -- output coordinate set of a strided sparse conv:
+ * every cell of the output grid whose receptive field (out*stride - pad +
+ * k*dil over all k) holds at least one input voxel of the same batch.  Output
+ * cells outside the output grid do not exist, so inputs that reach none are
+ * dropped (spconv docs, COMMON_PROBLEMS.md: shape [8,200,200], k3 s2 pad
+ * [0,1,1], the single point z=7 gives an empty output).  Rows are written
+ * sorted by (b, z, y, x).
+ *
+ *  out_shape   host out: the output grid (as spc_out_shape).
+ *  out_coords  [cap, 4] int32 out (16-byte aligned).
+ *  n_out       device int64 out: size of the output set, written even when it
+ *              exceeds cap (then SPC_ERR_CAPACITY is set in status and
+ *              out_coords holds only a prefix).
+ *  status      sticky error word: SPC_ERR_COORD_RANGE, SPC_ERR_CAPACITY.
+ *  ws          spc_strided_out_coords_workspace_size(n_in, g) bytes.
+ *  The caller reads n_out back to size the following buffers; cap = n_in * K
+ *  always suffices.
+ */
+SPC_API size_t spc_strided_out_coords_workspace_size(int64_t n_in, const spc_geom* g /*host*/);
+
+SPC_API spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, int32_t batch,
+                                  const int32_t in_shape[3] /*host*/, const spc_geom* g /*host*/,
+                                  int32_t out_shape[3] /*host, out*/, int32_t* out_coords,
+                                  int64_t cap, int64_t* n_out, int32_t* status, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------- conv
+ * spc_conv_fwd -- y[o, :] = bias + sum_k sum_{i = imap[k, o] != -1} x[i, :] W[k]
+ * (lato_mlx sparse/conv.py, module docstring: the output is the bias plus, over
+ * the kernel offsets, the weight slice times the feature of each occupied
+ * neighbour; absent neighbours add nothing).  One launch covers all offsets;
+ * each output row is written once (no atomics: results are run-to-run
+ * bit-identical).
+ *
+ *  x     [n_in, cin] of dtype dt.      w [K, cin, cout] of dtype dt.
+ *  bias  [cout] of dtype dt, or NULL.
+ *  imap  [K, n_out] int32, or NULL when K == 1 and n_in == n_out: the 1x1
+ *        submanifold conv is a per-voxel linear layer y = x W[0] + bias and
+ *        needs no map (lato_mlx sparse/conv.py, SubMConv3d.__call__ k=1
+ *        shortcut; HYGON-AI spconv-das README, 1x1 takes the GEMM path).
+ *  mask  [n_out] uint32 or NULL: the per-row offset mask from
+ *        spc_build_indice_map; lets tiles skip offsets no row of theirs uses.
+ *  y     [n_out, cout] of dtype dt out (fp32 accumulate, one rounding).
+ *  ws    spc_conv_workspace_size(...) bytes.
+ *  x, w, y must be 16-byte aligned.
+ */
+SPC_API size_t spc_conv_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
+                               int32_t cout, spc_dtype dt);
+
+SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
+                        const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
+                        int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec, void* y,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* spc_conv_dgrad -- dx[i, :] = sum over pairs imap[k, o] = i of W[k] dy[o, :]
+ * (the gradient of spc_conv_fwd with respect to x; "dinput" in the HYGON-AI
+ * spconv-das README, Testing and Accuracy).  Computed input-stationary through
+ * the transposed map, one write per row of dx, no atomics.
+ *
+ *  dy    [n_out, cout] of dtype dt.   w [K, cin, cout].
+ *  map   see spc_map_kind: imap_t [K, n_in] (SPC_MAP_TRANSPOSED) or the
+ *        submanifold imap [K, n] (SPC_MAP_SUBM_MIRROR, n_in == n_out); NULL
+ *        when K == 1 and n_in == n_out (dx = dy W[0]^T).
+ *  dx    [n_in, cin] of dtype dt out.
+ */
+SPC_API spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
+                          int32_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
+                          spc_dtype dt, spc_precision prec, void* dx, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* spc_conv_wgrad -- dW[k] = sum_{o: imap[k, o] = i != -1} x[i, :]^T dy[o, :],
+ * reduced in fp32 over all active pairs ("dfilter" in the HYGON-AI spconv-das
+ * README).  Split over fixed chunks of output rows and summed in a fixed
+ * order, so the result is run-to-run bit-identical.
+ *
+ *  x   [n_in, cin], dy [n_out, cout] of dtype dt;  imap [K, n_out] (NULL when
+ *      K == 1 and n_in == n_out).
+ *  dw  [K, cin, cout] float32 out (overwritten, not accumulated).
+ *  ws  spc_conv_wgrad_workspace_size(...) bytes.
+ */
+SPC_API size_t spc_conv_wgrad_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
+                                     int32_t cout, spc_dtype dt);
+
+SPC_API spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, int32_t K,
+                          int64_t n_in, int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
+                          spc_precision prec, float* dw, void* ws, size_t ws_bytes,
+                          void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPC_H */

@@ -1,0 +1,309 @@
+// api.cu -- the extern "C" entry points of libspc.so declared in include/spc.h.
+//
+// Each entry point checks its arguments on the host (returning an error before
+// anything is enqueued), carves the caller's workspace, and enqueues its
+// kernels on the caller's stream.  Nothing here allocates device memory or
+// synchronises.
+#include "kernels.cuh"
+
+using namespace spc;
+
+namespace {
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+
+bool geom_ok(const spc_geom* g, bool need_stride_pad)
+{
+    if (!g) return false;
+    for (int a = 0; a < 3; ++a) {
+        if (g->ksize[a] < 1 || g->dil[a] < 1) return false;
+        if (need_stride_pad && (g->stride[a] < 1 || g->pad[a] < 0)) return false;
+    }
+    return true;
+}
+
+int64_t kvol(const spc_geom* g) { return (int64_t)g->ksize[0] * g->ksize[1] * g->ksize[2]; }
+
+bool shape_ok(const int32_t s[3]) { return s && s[0] > 0 && s[1] > 0 && s[2] > 0; }
+
+int32_t axis_out(int32_t in, int32_t k, int32_t s, int32_t p, int32_t dil)
+{
+    const int64_t span = (int64_t)in + 2 * (int64_t)p - (int64_t)dil * (k - 1) - 1;
+    if (span < 0) return 0;
+    return (int32_t)(span / s + 1);
+}
+
+size_t table_bytes(int64_t n) { return align_up(sizeof(unsigned long long) * (size_t)hash_slots_for(n), 256); }
+
+int elem_bytes(spc_dtype dt) { return dt == SPC_F32 ? 4 : 2; }
+
+bool dtype_ok(spc_dtype dt) { return dt == SPC_F32 || dt == SPC_F16 || dt == SPC_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* spc_status_string(spc_status s)
+{
+    switch (s) {
+    case SPC_OK: return "ok";
+    case SPC_ERR_INVALID_ARG: return "invalid argument";
+    case SPC_ERR_COORD_RANGE: return "coordinate outside the batch or the grid";
+    case SPC_ERR_DUPLICATE: return "duplicate coordinate";
+    case SPC_ERR_TABLE_FULL: return "hash table probe bound exceeded";
+    case SPC_ERR_CAPACITY: return "output set larger than the output buffer";
+    case SPC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SPC_ERR_CUDA: return "CUDA runtime error";
+    case SPC_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int32_t spc_version(void) { return kVersion; }
+
+spc_status spc_out_shape(const int32_t in_shape[3], const spc_geom* g, int32_t out_shape[3])
+{
+    if (!shape_ok(in_shape) || !geom_ok(g, true) || !out_shape) return SPC_ERR_INVALID_ARG;
+    for (int a = 0; a < 3; ++a)
+        out_shape[a] = axis_out(in_shape[a], g->ksize[a], g->stride[a], g->pad[a], g->dil[a]);
+    return SPC_OK;
+}
+
+size_t spc_indice_map_workspace_size(int64_t n_in)
+{
+    return n_in < 0 ? 0 : table_bytes(n_in);
+}
+
+spc_status spc_build_indice_map(const int32_t* coords, int64_t n_in, int32_t batch,
+                                const int32_t in_shape[3], const spc_geom* g, int32_t subm,
+                                const int32_t* out_coords, int64_t n_out, int32_t* imap,
+                                int32_t* imap_t, int32_t* pair_count, uint32_t* mask,
+                                int32_t* status, void* ws, size_t ws_bytes, void* stream)
+{
+    if (n_in < 0 || n_out < 0 || batch < 1 || !shape_ok(in_shape) || !geom_ok(g, !subm))
+        return SPC_ERR_INVALID_ARG;
+    const int64_t K = kvol(g);
+    if (K > (1 << 20)) return SPC_ERR_INVALID_ARG;
+    if (!pair_count || !status) return SPC_ERR_INVALID_ARG;
+    if (mask && K > 32) return SPC_ERR_INVALID_ARG;
+    ProbeGeom pg;
+    pg.batch = batch;
+    pg.K = (int32_t)K;
+    int32_t out_shape[3];
+    if (subm) {
+        if (n_out != n_in || imap_t) return SPC_ERR_INVALID_ARG;
+        for (int a = 0; a < 3; ++a) {
+            if (g->ksize[a] % 2 != 1) return SPC_ERR_INVALID_ARG;
+            out_shape[a] = in_shape[a];
+            pg.stride[a] = 1;
+            pg.pad[a] = (g->ksize[a] / 2) * g->dil[a];
+        }
+        pg.centre = (int32_t)(K / 2);
+        out_coords = coords;
+    } else {
+        for (int a = 0; a < 3; ++a) {
+            out_shape[a] = axis_out(in_shape[a], g->ksize[a], g->stride[a], g->pad[a], g->dil[a]);
+            pg.stride[a] = g->stride[a];
+            pg.pad[a] = g->pad[a];
+        }
+        pg.centre = -1;
+        if (n_out > 0 && !out_coords) return SPC_ERR_INVALID_ARG;
+    }
+    for (int a = 0; a < 3; ++a) {
+        pg.in_shape[a] = in_shape[a];
+        pg.q_shape[a] = out_shape[a];
+        pg.ksize[a] = g->ksize[a];
+        pg.dil[a] = g->dil[a];
+    }
+    if (n_in > 0 && (!coords || !aligned16(coords))) return SPC_ERR_INVALID_ARG;
+    if (n_out > 0 && (!imap || !aligned16(out_coords))) return SPC_ERR_INVALID_ARG;
+    if (n_in > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    const unsigned __int128 cells = (unsigned __int128)batch * (unsigned)in_shape[0] *
+                                    (unsigned)in_shape[1] * (unsigned)in_shape[2];
+    const int vbits = hash_vbits_for(n_in);
+    if (cells > (unsigned __int128)INT64_MAX || !hash_keys_fit((int64_t)cells, vbits))
+        return SPC_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < spc_indice_map_workspace_size(n_in)) return SPC_ERR_WORKSPACE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SPC_CUDA_TRY(cudaMemsetAsync(pair_count, 0, sizeof(int32_t) * (size_t)K, st));
+    if (imap_t && n_in > 0) SPC_CUDA_TRY(cudaMemsetAsync(imap_t, 0xFF, sizeof(int32_t) * (size_t)(K * n_in), st));
+    if (n_out == 0 && n_in == 0) return SPC_OK;
+
+    HashTable t;
+    t.slots = static_cast<unsigned long long*>(ws);
+    t.log2_buckets = ceil_log2((uint64_t)hash_slots_for(n_in)) - 2;
+    t.vbits = vbits;
+    spc_status s = hash_clear(t, st);
+    if (s != SPC_OK) return s;
+    s = hash_insert(coords, n_in, batch, in_shape, t, status, st);
+    if (s != SPC_OK) return s;
+    return map_probe(out_coords, n_out, n_in, pg, t, imap, imap_t, pair_count, mask, status, st);
+}
+
+size_t spc_strided_out_coords_workspace_size(int64_t n_in, const spc_geom* g)
+{
+    if (n_in < 0 || !geom_ok(g, true)) return 0;
+    return outcoords_ws_bytes(n_in, (int32_t)kvol(g));
+}
+
+spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, int32_t batch,
+                                  const int32_t in_shape[3], const spc_geom* g,
+                                  int32_t out_shape[3], int32_t* out_coords, int64_t cap,
+                                  int64_t* n_out, int32_t* status, void* ws, size_t ws_bytes,
+                                  void* stream)
+{
+    if (n_in < 0 || cap < 0 || batch < 1 || !shape_ok(in_shape) || !geom_ok(g, true) ||
+        !out_shape || !n_out || !status)
+        return SPC_ERR_INVALID_ARG;
+    const int64_t K = kvol(g);
+    if (K > (1 << 20)) return SPC_ERR_INVALID_ARG;
+    if (n_in > 0 && (!coords || !aligned16(coords))) return SPC_ERR_INVALID_ARG;
+    if (cap > 0 && (!out_coords || !aligned16(out_coords))) return SPC_ERR_INVALID_ARG;
+    for (int a = 0; a < 3; ++a)
+        out_shape[a] = axis_out(in_shape[a], g->ksize[a], g->stride[a], g->pad[a], g->dil[a]);
+    if (n_in * K > (int64_t)UINT32_MAX) return SPC_ERR_UNSUPPORTED;
+    const unsigned __int128 out_cells = (unsigned __int128)batch * (unsigned)out_shape[0] *
+                                        (unsigned)out_shape[1] * (unsigned)out_shape[2];
+    if (out_cells > (unsigned __int128)INT64_MAX) return SPC_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < spc_strided_out_coords_workspace_size(n_in, g)) return SPC_ERR_WORKSPACE;
+    ProbeGeom pg;
+    for (int a = 0; a < 3; ++a) {
+        pg.in_shape[a] = in_shape[a];
+        pg.q_shape[a] = out_shape[a];
+        pg.ksize[a] = g->ksize[a];
+        pg.stride[a] = g->stride[a];
+        pg.pad[a] = g->pad[a];
+        pg.dil[a] = g->dil[a];
+    }
+    pg.batch = batch;
+    pg.K = (int32_t)K;
+    pg.centre = -1;
+    return strided_out_coords(coords, n_in, pg, out_shape, out_coords, cap, n_out, status, ws,
+                              ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t spc_conv_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
+                               spc_dtype dt)
+{
+    (void)K;
+    (void)n_in;
+    (void)n_out;
+    (void)cin;
+    (void)cout;
+    (void)dt;
+    return 0;
+}
+
+namespace {
+
+spc_status check_conv(const void* a, const void* w, const void* out, int32_t K, int64_t n_a,
+                      int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt)
+{
+    if (!dtype_ok(dt) || K < 1 || n_a < 0 || n_out < 0 || cin < 1 || cout < 1)
+        return SPC_ERR_INVALID_ARG;
+    if (!w || !aligned16(w)) return SPC_ERR_INVALID_ARG;
+    if (n_a > 0 && (!a || !aligned16(a))) return SPC_ERR_INVALID_ARG;
+    if (n_out > 0 && (!out || !aligned16(out))) return SPC_ERR_INVALID_ARG;
+    if (n_a > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    (void)elem_bytes;
+    return SPC_OK;
+}
+
+}  // namespace
+
+spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
+                        const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
+                        int32_t cout, spc_dtype dt, spc_precision prec, void* y, void* ws,
+                        size_t ws_bytes, void* stream)
+{
+    (void)ws;
+    (void)ws_bytes;
+    spc_status s = check_conv(x, w, y, K, n_in, n_out, cin, cout, dt);
+    if (s != SPC_OK) return s;
+    if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
+    if (!imap && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if (mask && K > 32) return SPC_ERR_INVALID_ARG;
+    GatherGemm p;
+    p.in = x;
+    p.w = w;
+    p.bias = bias;
+    p.map = imap;
+    p.mask = mask;
+    p.out = y;
+    p.rows = n_out;
+    p.in_rows = n_in;
+    p.K = K;
+    p.cred = cin;
+    p.cout = cout;
+    p.mirror = 0;
+    p.transpose_w = 0;
+    return conv_gather_simt(p, dt, static_cast<cudaStream_t>(stream));
+}
+
+spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
+                          int32_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
+                          spc_dtype dt, spc_precision prec, void* dx, void* ws, size_t ws_bytes,
+                          void* stream)
+{
+    (void)ws;
+    (void)ws_bytes;
+    spc_status s = check_conv(dy, w, dx, K, n_out, n_in, cin, cout, dt);
+    if (s != SPC_OK) return s;
+    if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
+    if (kind != SPC_MAP_TRANSPOSED && kind != SPC_MAP_SUBM_MIRROR) return SPC_ERR_INVALID_ARG;
+    if (kind == SPC_MAP_SUBM_MIRROR && n_in != n_out) return SPC_ERR_INVALID_ARG;
+    if (!map && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    GatherGemm p;
+    p.in = dy;
+    p.w = w;
+    p.bias = nullptr;
+    p.map = map;
+    p.mask = nullptr;
+    p.out = dx;
+    p.rows = n_in;
+    p.in_rows = n_out;
+    p.K = K;
+    p.cred = cout;
+    p.cout = cin;
+    p.mirror = (kind == SPC_MAP_SUBM_MIRROR) ? 1 : 0;
+    p.transpose_w = 1;
+    return conv_gather_simt(p, dt, static_cast<cudaStream_t>(stream));
+}
+
+size_t spc_conv_wgrad_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
+                                     int32_t cout, spc_dtype dt)
+{
+    (void)n_in;
+    (void)dt;
+    if (K < 1 || n_out < 0 || cin < 1 || cout < 1) return 0;
+    return wgrad_ws_bytes(K, n_out, cin, cout);
+}
+
+spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, int32_t K,
+                          int64_t n_in, int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
+                          spc_precision prec, float* dw, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!dtype_ok(dt) || K < 1 || n_in < 0 || n_out < 0 || cin < 1 || cout < 1 || !dw)
+        return SPC_ERR_INVALID_ARG;
+    if (n_in > 0 && (!x || !aligned16(x))) return SPC_ERR_INVALID_ARG;
+    if (n_out > 0 && (!dy || !aligned16(dy))) return SPC_ERR_INVALID_ARG;
+    if (n_in > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
+    if (!imap && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if (ws_bytes < spc_conv_wgrad_workspace_size(K, n_in, n_out, cin, cout, dt) || !ws)
+        return SPC_ERR_WORKSPACE;
+    WgradArgs a;
+    a.x = x;
+    a.dy = dy;
+    a.map = imap;
+    a.dw = dw;
+    a.n_in = n_in;
+    a.n_out = n_out;
+    a.K = K;
+    a.cin = cin;
+    a.cout = cout;
+    return conv_wgrad_simt(a, dt, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// kernels.cuh -- internal launch interfaces between the C ABI (api.cu) and the
+// kernel translation units.  Everything here is device-side work enqueued on a
+// stream; argument validation happens in api.cu before these are called.
+#pragma once
+
+#include "common.cuh"
+
+namespace spc {
+
+// ------------------------------------------------------------------ hash table
+// Open addressing over 32-byte buckets of four 64-bit slots.  A slot holds
+// (cell key << vbits) | row, or all ones when empty.  A 4-lane group of a warp
+// reads one bucket per step (one L2 sector) and resolves the probe with a
+// ballot; buckets are visited linearly from the key's multiplicative hash.
+struct HashTable {
+    unsigned long long* slots;  // [4 << log2_buckets]
+    int log2_buckets;
+    int vbits;                  // bits of the row field
+};
+
+// Number of 64-bit slots a table for n keys uses (load factor <= 1/2).
+int64_t hash_slots_for(int64_t n);
+
+// vbits for n rows, and whether every key of a grid of `cells` cells fits beside it.
+int hash_vbits_for(int64_t n);
+bool hash_keys_fit(int64_t cells, int vbits);
+
+// Geometry of a probe: the cell read by query row o through offset index
+// (a, b, c) is q*stride - pad + (a, b, c)*dil per axis.
+struct ProbeGeom {
+    int32_t in_shape[3];   // grid of the table's cells
+    int32_t q_shape[3];    // grid the query coordinates must lie in
+    int32_t ksize[3];
+    int32_t stride[3];
+    int32_t pad[3];
+    int32_t dil[3];
+    int32_t batch;
+    int32_t K;
+    int32_t centre;        // offset index that maps each row to itself (subm), or -1
+};
+
+spc_status hash_clear(HashTable t, cudaStream_t st);
+spc_status hash_insert(const int32_t* coords, int64_t n, int32_t batch, const int32_t shape[3],
+                       HashTable t, int32_t* status, cudaStream_t st);
+spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const ProbeGeom& g,
+                     HashTable t, int32_t* imap, int32_t* imap_t, int32_t* pair_count,
+                     uint32_t* mask, int32_t* status, cudaStream_t st);
+
+// ------------------------------------------------------ strided output coords
+size_t outcoords_ws_bytes(int64_t n_in, int32_t K);
+spc_status strided_out_coords(const int32_t* coords, int64_t n_in, const ProbeGeom& g,
+                              const int32_t out_shape[3], int32_t* out_coords, int64_t cap,
+                              int64_t* n_out, int32_t* status, void* ws, size_t ws_bytes,
+                              cudaStream_t st);
+
+// ------------------------------------------------------------------ conv SIMT
+// Gathered implicit GEMM on CUDA cores:
+//   out[r, j] = bias[j] + sum_k sum_c in[map(k, r), c] * B(k, c, j)
+// with map(k, r) = map[mk * rows + r] (mk = k, or K-1-k when mirror), or r when
+// map == NULL (K == 1), and B(k, c, j) = w[k][c][j], or w[k][j][c] when
+// transpose_w.  `cred` is the reduction width (columns of `in`), `cout` the
+// output width; the weight tensor is [K][cred][cout], or [K][cout][cred] when
+// transposed.
+struct GatherGemm {
+    const void* in;
+    const void* w;
+    const void* bias;
+    const int32_t* map;
+    const uint32_t* mask;   // per output row, bit k = map(k, r) != -1 (or NULL)
+    void* out;
+    int64_t rows;           // output rows
+    int64_t in_rows;
+    int32_t K;
+    int32_t cred;
+    int32_t cout;
+    int32_t mirror;
+    int32_t transpose_w;
+};
+spc_status conv_gather_simt(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
+
+// dW[k] = sum_o x[map[k,o]]^T dy[o] in fp32, deterministic split over output rows.
+struct WgradArgs {
+    const void* x;
+    const void* dy;
+    const int32_t* map;
+    float* dw;
+    int64_t n_in, n_out;
+    int32_t K, cin, cout;
+};
+size_t wgrad_ws_bytes(int32_t K, int64_t n_out, int32_t cin, int32_t cout);
+spc_status conv_wgrad_simt(const WgradArgs& a, spc_dtype dt, void* ws, size_t ws_bytes,
+                           cudaStream_t st);
+
+}  // namespace spc

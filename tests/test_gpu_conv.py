@@ -1,0 +1,177 @@
+"""GPU parity of the convolution kernels against the fp64 oracle.
+
+Floating-point results are compared normwise, ||gpu - oracle|| / ||oracle||,
+within 1e-5 (fp32 exact), 2e-3 (tf32) and 2e-2 (fp16 / bf16).  Small cases
+are compared in full; the full-size workloads on sampled rows (first and last
+tiles, the ragged tail, and random rows) or sampled dW entries, which the
+oracle computes one by one.  Run-to-run bit identity is checked too."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scenes
+import sparse_convolution_hash_gb300 as spc
+from gpu_util import TOL, DT, dev, normwise, rand_coords, rand_tensor, sample_rows, to_np
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = {"uniform32": (32, 32, 32), "lidar": (41, 1600, 1408), "shell256": (256, 256, 256),
+          "shell192x4": (192, 192, 192)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def subm_case(coords, batch, shape, cin, cout, dtype, ks=3, seed=0, bias=True):
+    g = np.random.default_rng(seed)
+    n = coords.shape[0]
+    K = ks ** 3
+    x = rand_tensor(g, (n, cin), dtype)
+    w = rand_tensor(g, (K, cin, cout), dtype, std=float(np.sqrt(1.0 / (K * cin))))
+    b = rand_tensor(g, (cout,), dtype, std=0.1) if bias else None
+    dy = rand_tensor(g, (n, cout), dtype)
+    m = spc.spc_build_indice_map(torch.from_numpy(coords).to(dev()), batch, shape, ksize=ks)
+    spc.check_status(m["status"])
+    imap_ref, _ = oracle.subm_map(coords, batch, shape, ks)
+    return x, w, b, dy, m, imap_ref
+
+
+@pytest.mark.parametrize("dtype,prec", [("f32", "exact"), ("f32", "tf32"), ("f16", "exact"),
+                                        ("bf16", "exact")])
+@pytest.mark.parametrize("n,cin,cout", [(1, 8, 8), (777, 16, 16), (1500, 24, 40),
+                                        (2100, 64, 128), (900, 128, 96)])
+def test_subm_small_full(dtype, prec, n, cin, cout):
+    g = np.random.default_rng(n)
+    batch, shape = 2, (12, 11, 13)
+    coords = rand_coords(g, n, batch, shape)
+    x, w, b, dy, m, imap_ref = subm_case(coords, batch, shape, cin, cout, dtype, seed=n)
+    p = spc.SPC_PREC_TF32 if prec == "tf32" else spc.SPC_PREC_EXACT
+    d = dev()
+    tol = TOL[(dtype, prec)]
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], m["mask"], precision=p)
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, imap_ref)) < tol
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, precision=p)
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, n)) < tol
+    dw = spc.spc_conv_wgrad(x.to(d), dy.to(d), m["imap"], 27, precision=p)
+    assert normwise(to_np(dw), oracle.conv_wgrad(x, dy, imap_ref)) < tol
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_k1_gemm_shortcut(dtype):
+    g = np.random.default_rng(5)
+    n, cin, cout = 1234, 32, 48
+    x = rand_tensor(g, (n, cin), dtype)
+    w = rand_tensor(g, (1, cin, cout), dtype, std=0.2)
+    b = rand_tensor(g, (cout,), dtype, std=0.1)
+    d = dev()
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), None)
+    ref = x.double().numpy() @ w[0].double().numpy() + b.double().numpy()
+    assert normwise(to_np(y), ref) < TOL[(dtype, "exact")]
+    dy = rand_tensor(g, (n, cout), dtype)
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), None, spc.SPC_MAP_TRANSPOSED, n)
+    assert normwise(to_np(dx), dy.double().numpy() @ w[0].double().numpy().T) < TOL[(dtype, "exact")]
+    dw = spc.spc_conv_wgrad(x.to(d), dy.to(d), None, 1)
+    assert normwise(to_np(dw)[0], x.double().numpy().T @ dy.double().numpy()) < TOL[(dtype, "exact")]
+
+
+def test_uniform32_subm_f32_full():
+    """2,000 voxels in 32^3, fp32 16->16 with bias: the whole output at 1e-5."""
+    w = scenes.workload("uniform32_subm_f32")
+    d = dev()
+    m = spc.spc_build_indice_map(torch.from_numpy(w["coords"]).to(d), 1, (32, 32, 32))
+    spc.check_status(m["status"])
+    imap_ref, _ = oracle.subm_map(w["coords"], 1, (32, 32, 32))
+    y = spc.spc_conv_fwd(w["x"].to(d), w["w"].to(d), w["bias"].to(d), m["imap"], m["mask"])
+    assert normwise(to_np(y), oracle.conv_fwd(w["x"], w["w"], w["bias"], imap_ref)) < 1e-5
+    y2 = spc.spc_conv_fwd(w["x"].to(d), w["w"].to(d), w["bias"].to(d), m["imap"], m["mask"])
+    assert torch.equal(y, y2)
+
+
+def test_uniform32_strided_bf16():
+    """k3 s2 p1 on the 2,000-voxel set, bf16 64->128: fwd, dinput, dfilter in full."""
+    w = scenes.workload("uniform32_strided_bf16")
+    c = w["coords"]
+    d = dev()
+    dc = torch.from_numpy(c).to(d)
+    oc, _ = spc.spc_strided_out_coords(dc, 1, (32, 32, 32), 3, 2, 1, 1)
+    m = spc.spc_build_indice_map(dc, 1, (32, 32, 32), ksize=3, stride=2, pad=1, subm=False,
+                                 out_coords=oc, with_transpose=True)
+    spc.check_status(m["status"])
+    oc_ref = oracle.strided_out_coords(c, 1, (32, 32, 32), 3, 2, 1, 1)
+    imap_ref, imap_t_ref, _ = oracle.strided_map(c, oc_ref, 1, (32, 32, 32), 3, 2, 1, 1)
+    y = spc.spc_conv_fwd(w["x"].to(d), w["w"].to(d), None, m["imap"], m["mask"])
+    assert normwise(to_np(y), oracle.conv_fwd(w["x"], w["w"], None, imap_ref)) < 2e-2
+    g = np.random.default_rng(3)
+    dy = rand_tensor(g, (oc.shape[0], 128), "bf16")
+    dx = spc.spc_conv_dgrad(dy.to(d), w["w"].to(d), m["imap_t"], spc.SPC_MAP_TRANSPOSED, c.shape[0])
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w["w"], imap_ref, c.shape[0])) < 2e-2
+    dw = spc.spc_conv_wgrad(w["x"].to(d), dy.to(d), m["imap"], 27)
+    assert normwise(to_np(dw), oracle.conv_wgrad(w["x"], dy, imap_ref)) < 2e-2
+
+
+@pytest.mark.parametrize("name", ["lidar_subm_f16", "shell256_subm_bf16", "shell256_k1_bf16"])
+def test_forward_workloads_sampled(name):
+    w = scenes.workload(name)
+    c = w["coords"]
+    kind = name.split("_")[0]
+    batch, shape = int(c[:, 0].max()) + 1, SHAPES[kind]
+    ks = w["k"]
+    d = dev()
+    imap_ref, _ = oracle.subm_map(c, batch, shape, ks)
+    if ks == 1:
+        imap_dev, mask = None, None
+    else:
+        m = spc.spc_build_indice_map(torch.from_numpy(c).to(d), batch, shape, ksize=ks)
+        spc.check_status(m["status"])
+        imap_dev, mask = m["imap"], m["mask"]
+    x, wt = w["x"].to(d), w["w"].to(d)
+    b = w["bias"].to(d) if w["bias"] is not None else None
+    y = spc.spc_conv_fwd(x, wt, b, imap_dev, mask, n_out=c.shape[0])
+    rows = sample_rows(c.shape[0])
+    ref = oracle.conv_fwd(w["x"], w["w"], w["bias"], imap_ref, rows=rows)
+    assert normwise(to_np(y[torch.from_numpy(rows).to(d)]), ref) < TOL[(w["dtype"], "exact")]
+    y2 = spc.spc_conv_fwd(x, wt, b, imap_dev, mask, n_out=c.shape[0])
+    assert torch.equal(y, y2)
+
+
+def test_training_step_shell192x4_sampled():
+    """4 x 192^3 shells, bf16 64->64: fwd, dinput (mirror map) and dfilter."""
+    w = scenes.workload("shell192x4_train_bf16")
+    c = w["coords"]
+    n = c.shape[0]
+    d = dev()
+    m = spc.spc_build_indice_map(torch.from_numpy(c).to(d), 4, (192, 192, 192))
+    spc.check_status(m["status"])
+    imap_ref, _ = oracle.subm_map(c, 4, (192, 192, 192))
+    x, wt, dy = w["x"].to(d), w["w"].to(d), w["dy"].to(d)
+    y = spc.spc_conv_fwd(x, wt, None, m["imap"], m["mask"])
+    dx = spc.spc_conv_dgrad(dy, wt, m["imap"], spc.SPC_MAP_SUBM_MIRROR, n)
+    dw = spc.spc_conv_wgrad(x, dy, m["imap"], 27)
+    rows = sample_rows(n, seed=1)
+    r = torch.from_numpy(rows).to(d)
+    assert normwise(to_np(y[r]), oracle.conv_fwd(w["x"], w["w"], None, imap_ref, rows=rows)) < 2e-2
+    imap_t_ref = oracle.transpose_map(imap_ref, n)
+    assert normwise(to_np(dx[r]), oracle.conv_dgrad_rows(w["dy"], w["w"], imap_t_ref, rows)) < 2e-2
+    g = np.random.default_rng(2)
+    ent = np.unique(np.concatenate([np.arange(64), g.integers(0, 27 * 64 * 64, size=400)]))
+    ref = oracle.conv_wgrad_entries(w["x"], w["dy"], imap_ref, ent)
+    assert normwise(to_np(dw).reshape(-1)[ent], ref) < 2e-2
+    dw2 = spc.spc_conv_wgrad(x, dy, m["imap"], 27)
+    dx2 = spc.spc_conv_dgrad(dy, wt, m["imap"], spc.SPC_MAP_SUBM_MIRROR, n)
+    assert torch.equal(dw, dw2) and torch.equal(dx, dx2)
+
+
+def test_empty_conv():
+    d = dev()
+    x = torch.zeros((0, 16), dtype=torch.bfloat16, device=d)
+    w = torch.zeros((27, 16, 16), dtype=torch.bfloat16, device=d)
+    imap = torch.zeros((27, 0), dtype=torch.int32, device=d)
+    assert spc.spc_conv_fwd(x, w, None, imap).shape == (0, 16)
+    dw = spc.spc_conv_wgrad(x, torch.zeros((0, 16), dtype=torch.bfloat16, device=d), imap, 27)
+    assert (dw == 0).all()
