@@ -222,7 +222,7 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
     spc_status s = check_conv(x, w, y, K, n_in, n_out, cin, cout, dt);
     if (s != SPC_OK) return s;
     if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
-    if (!imap && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if (!imap && n_out > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
     if (mask && K > 32) return SPC_ERR_INVALID_ARG;
     GatherGemm p;
     p.in = x;
@@ -253,7 +253,7 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
     if (kind != SPC_MAP_TRANSPOSED && kind != SPC_MAP_SUBM_MIRROR) return SPC_ERR_INVALID_ARG;
     if (kind == SPC_MAP_SUBM_MIRROR && n_in != n_out) return SPC_ERR_INVALID_ARG;
-    if (!map && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if (!map && n_in > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
     GatherGemm p;
     p.in = dy;
     p.w = w;
@@ -290,7 +290,7 @@ spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, in
     if (n_out > 0 && (!dy || !aligned16(dy))) return SPC_ERR_INVALID_ARG;
     if (n_in > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
     if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
-    if (!imap && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if (!imap && n_out > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
     if (ws_bytes < spc_conv_wgrad_workspace_size(K, n_in, n_out, cin, cout, dt) || !ws)
         return SPC_ERR_WORKSPACE;
     WgradArgs a;

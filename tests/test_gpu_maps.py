@@ -45,7 +45,7 @@ def check_subm(coords, batch, shape, ks=3, dil=1):
     (7, 1, (4, 4, 4), 3, 1),
     (333, 2, (9, 8, 7), 3, 1),
     (1000, 3, (10, 10, 10), (3, 1, 5), (1, 2, 1)),
-    (2501, 1, (17, 13, 11), 5, 1),
+    (2501, 1, (17, 13, 13), 5, 1),
     (64, 1, (4, 4, 4), 3, 1),          # every cell of the grid occupied
     (500, 2, (12, 12, 12), 1, 1),
 ])
