@@ -142,6 +142,35 @@ SPC_API spc_status spc_build_indice_map(const int32_t* coords, int64_t n_in, int
                                 uint32_t* mask, int32_t* status, void* ws, size_t ws_bytes,
                                 void* stream);
 
+/* spc_build_indice_map_noalloc -- the same indice-map build as
+ * spc_build_indice_map, for callers that cannot allocate device memory: an
+ * inference engine's enqueue step that must not call cudaMalloc/cudaFree
+ * (they can stall the whole device), a host framework that owns all device
+ * memory through its own pool and offers no workspace, or a latency-bound loop
+ * that sized every buffer at start-up.  The pages describe no such variant;
+ * it has no counterpart there.
+ *
+ *  Arguments are those of spc_build_indice_map without ws / ws_bytes; the hash
+ *  table lives instead in a 16 MiB array of device memory inside the library,
+ *  which every GPU that loads the library keeps until the process exits.
+ *  n_in may be at most SPC_NOALLOC_MAX_VOXELS; larger inputs return
+ *  SPC_ERR_WORKSPACE before any work is enqueued.
+ *  The first call on a device looks up the array's device address (once per
+ *  device, with that device current); make that first call before any stream
+ *  capture.  The call allocates nothing and synchronises nothing.
+ *  All calls on a device share the one table.  Each call clears it before use,
+ *  but calls whose GPU work overlaps (other streams, other host threads) race
+ *  on it: the caller must serialise them. */
+#define SPC_NOALLOC_MAX_VOXELS 1048576
+
+SPC_API spc_status spc_build_indice_map_noalloc(const int32_t* coords, int64_t n_in,
+                                                int32_t batch, const int32_t in_shape[3] /*host*/,
+                                                const spc_geom* g /*host*/, int32_t subm,
+                                                const int32_t* out_coords, int64_t n_out,
+                                                int32_t* imap, int32_t* imap_t,
+                                                int32_t* pair_count, uint32_t* mask,
+                                                int32_t* status, void* stream);
+
 /* ------------------------------------------------------ strided output coords
  * spc_strided_out_coords -- output coordinate set of a strided sparse conv:
  * every cell of the output grid whose receptive field (out*stride - pad +
