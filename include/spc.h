@@ -235,12 +235,16 @@ SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, 
  *  map   see spc_map_kind: imap_t [K, n_in] (SPC_MAP_TRANSPOSED) or the
  *        submanifold imap [K, n] (SPC_MAP_SUBM_MIRROR, n_in == n_out); NULL
  *        when K == 1 and n_in == n_out (dx = dy W[0]^T).
+ *  mask  NULL, or with SPC_MAP_SUBM_MIRROR (K <= 32) the row mask that
+ *        spc_build_indice_map wrote for that submanifold map (the kernel
+ *        mirrors its bits itself).
  *  dx    [n_in, cin] of dtype dt out.
  */
-SPC_API spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
-                          int32_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
-                          spc_dtype dt, spc_precision prec, void* dx, void* ws, size_t ws_bytes,
-                          void* stream);
+SPC_API spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map,
+                                  spc_map_kind kind, const uint32_t* mask, int32_t K, int64_t n_in,
+                                  int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
+                                  spc_precision prec, void* dx, void* ws, size_t ws_bytes,
+                                  void* stream);
 
 /* spc_conv_wgrad -- dW[k] = sum_{o: imap[k, o] = i != -1} x[i, :]^T dy[o, :],
  * reduced in fp32 over all active pairs ("dfilter" in the HYGON-AI spconv-das

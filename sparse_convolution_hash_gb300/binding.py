@@ -107,8 +107,8 @@ def lib():
             L.spc_conv_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
                                        _i32, _p, _p, _sz, _p]
             L.spc_conv_fwd.restype = _i32
-            L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _i32, _i64, _i64, _i32, _i32, _i32,
-                                         _i32, _p, _p, _sz, _p]
+            L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _i32, _i64, _i64, _i32, _i32,
+                                         _i32, _i32, _p, _p, _sz, _p]
             L.spc_conv_dgrad.restype = _i32
             L.spc_conv_wgrad_workspace_size.argtypes = [_i32, _i64, _i64, _i32, _i32, _i32]
             L.spc_conv_wgrad_workspace_size.restype = _sz
@@ -177,11 +177,13 @@ def spc_build_indice_map(coords: torch.Tensor, batch: int, in_shape: Sequence[in
                          stride=1, pad=0, dil=1, subm: bool = True,
                          out_coords: Optional[torch.Tensor] = None, with_transpose: bool = False,
                          with_mask: bool = True, status: Optional[torch.Tensor] = None,
-                         ws: Optional[torch.Tensor] = None) -> dict:
+                         ws: Optional[torch.Tensor] = None, out: Optional[dict] = None) -> dict:
     """Indice map [K, N_out] (+ transpose [K, N_in], pair counts [K], row masks [N_out]).
 
     Returns a dict with keys imap, imap_t (or None), pair_count, mask (or None),
-    status.  Data errors land in `status`; call check_status() to raise them.
+    status, ws.  Data errors land in `status`; call check_status() to raise them.
+    Passing the dict of an earlier call as `out` reuses its buffers (no
+    allocation, so the call can be captured in a CUDA graph).
     """
     coords = _cuda(coords, "coords").to(torch.int32)
     dev = coords.device
@@ -194,10 +196,16 @@ def spc_build_indice_map(coords: torch.Tensor, batch: int, in_shape: Sequence[in
     else:
         oc = _cuda(out_coords, "out_coords").to(torch.int32)
         n_out = oc.shape[0]
-    imap = torch.empty((K, n_out), dtype=torch.int32, device=dev)
-    imap_t = torch.empty((K, n_in), dtype=torch.int32, device=dev) if (with_transpose and not subm) else None
-    pair_count = torch.empty(K, dtype=torch.int32, device=dev)
-    mask = torch.empty(n_out, dtype=torch.int32, device=dev) if (with_mask and K <= 32) else None
+    if out is not None:
+        imap, imap_t, pair_count, mask = out["imap"], out["imap_t"], out["pair_count"], out["mask"]
+        status = out["status"] if status is None else status
+        ws = out["ws"] if ws is None else ws
+    else:
+        imap = torch.empty((K, n_out), dtype=torch.int32, device=dev)
+        imap_t = (torch.empty((K, n_in), dtype=torch.int32, device=dev)
+                  if (with_transpose and not subm) else None)
+        pair_count = torch.empty(K, dtype=torch.int32, device=dev)
+        mask = torch.empty(n_out, dtype=torch.int32, device=dev) if (with_mask and K <= 32) else None
     status = new_status(dev) if status is None else status
     nbytes = spc_indice_map_workspace_size(n_in)
     if ws is None or ws.numel() < nbytes:
@@ -263,31 +271,35 @@ def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
 
 
 def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tensor], kind: int,
-                   n_in: int, precision: int = SPC_PREC_EXACT) -> torch.Tensor:
+                   n_in: int, precision: int = SPC_PREC_EXACT, mask: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """dx[i] = sum over pairs imap[k, o] = i of W[k] dy[o]."""
     dy = _cuda(dy, "dy")
     w = _cuda(w, "w").to(dy.dtype)
     K, cin, cout = w.shape
     m = _cuda(map_, "map") if map_ is not None else None
-    dx = torch.empty((n_in, cin), dtype=dy.dtype, device=dy.device)
+    dx = torch.empty((n_in, cin), dtype=dy.dtype, device=dy.device) if out is None else out
     dt = _DTYPES[dy.dtype]
-    code = lib().spc_conv_dgrad(_ptr(dy), _ptr(w), _ptr(m), kind, K, n_in, dy.shape[0], cin, cout,
-                                dt, precision, _ptr(dx), None, 0, _stream(dy.device))
+    code = lib().spc_conv_dgrad(_ptr(dy), _ptr(w), _ptr(m), kind, _ptr(mask), K, n_in,
+                                dy.shape[0], cin, cout, dt, precision, _ptr(dx), None, 0,
+                                _stream(dy.device))
     _check(code, "spc_conv_dgrad")
     return dx
 
 
 def spc_conv_wgrad(x: torch.Tensor, dy: torch.Tensor, imap: Optional[torch.Tensor], K: int,
-                   precision: int = SPC_PREC_EXACT) -> torch.Tensor:
+                   precision: int = SPC_PREC_EXACT, out: Optional[torch.Tensor] = None,
+                   ws: Optional[torch.Tensor] = None) -> torch.Tensor:
     """dW[k] = sum over pairs of x[imap[k, o]]^T dy[o], float32 [K, cin, cout]."""
     x = _cuda(x, "x")
     dy = _cuda(dy, "dy").to(x.dtype)
     m = _cuda(imap, "imap") if imap is not None else None
     cin, cout = x.shape[1], dy.shape[1]
-    dw = torch.empty((K, cin, cout), dtype=torch.float32, device=x.device)
+    dw = torch.empty((K, cin, cout), dtype=torch.float32, device=x.device) if out is None else out
     dt = _DTYPES[x.dtype]
     nbytes = int(lib().spc_conv_wgrad_workspace_size(K, x.shape[0], dy.shape[0], cin, cout, dt))
-    ws = _workspace(nbytes, x.device)
+    if ws is None or ws.numel() < nbytes:
+        ws = _workspace(nbytes, x.device)
     code = lib().spc_conv_wgrad(_ptr(x), _ptr(dy), _ptr(m), K, x.shape[0], dy.shape[0], cin, cout,
                                 dt, precision, _ptr(dw), _ptr(ws), ws.numel(), _stream(x.device))
     _check(code, "spc_conv_wgrad")

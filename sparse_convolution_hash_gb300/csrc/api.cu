@@ -210,6 +210,17 @@ spc_status check_conv(const void* a, const void* w, const void* out, int32_t K, 
     return SPC_OK;
 }
 
+// Picks the conv kernel for a gathered GEMM: the narrow-channel kernel when the
+// channel widths allow it, else the general tiled CUDA-core kernel.
+spc_status run_gather(const GatherGemm& p, spc_dtype dt, cudaStream_t st)
+{
+    if (conv_narrow_supported(p.cred, p.cout, p.K, dt) && aligned16(p.in) && aligned16(p.out)) {
+        const spc_status s = conv_gather_narrow(p, dt, st);
+        if (s != SPC_ERR_UNSUPPORTED) return s;
+    }
+    return conv_gather_simt(p, dt, st);
+}
+
 }  // namespace
 
 spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
@@ -238,13 +249,13 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
     p.cout = cout;
     p.mirror = 0;
     p.transpose_w = 0;
-    return conv_gather_simt(p, dt, static_cast<cudaStream_t>(stream));
+    return run_gather(p, dt, static_cast<cudaStream_t>(stream));
 }
 
 spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
-                          int32_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
-                          spc_dtype dt, spc_precision prec, void* dx, void* ws, size_t ws_bytes,
-                          void* stream)
+                          const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
+                          int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec, void* dx,
+                          void* ws, size_t ws_bytes, void* stream)
 {
     (void)ws;
     (void)ws_bytes;
@@ -254,12 +265,13 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     if (kind != SPC_MAP_TRANSPOSED && kind != SPC_MAP_SUBM_MIRROR) return SPC_ERR_INVALID_ARG;
     if (kind == SPC_MAP_SUBM_MIRROR && n_in != n_out) return SPC_ERR_INVALID_ARG;
     if (!map && n_in > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if (mask && (K > 32 || kind != SPC_MAP_SUBM_MIRROR)) return SPC_ERR_INVALID_ARG;
     GatherGemm p;
     p.in = dy;
     p.w = w;
     p.bias = nullptr;
     p.map = map;
-    p.mask = nullptr;
+    p.mask = mask;
     p.out = dx;
     p.rows = n_in;
     p.in_rows = n_out;
@@ -268,7 +280,7 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     p.cout = cin;
     p.mirror = (kind == SPC_MAP_SUBM_MIRROR) ? 1 : 0;
     p.transpose_w = 1;
-    return conv_gather_simt(p, dt, static_cast<cudaStream_t>(stream));
+    return run_gather(p, dt, static_cast<cudaStream_t>(stream));
 }
 
 size_t spc_conv_wgrad_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,

@@ -6,10 +6,13 @@
 // explicit range check instead of a pad shift).  A slot packs the key above the
 // row index, so one 8-byte read both matches and resolves a probe.
 //
-// Warp-cooperative probing: four lanes own one query and read the four slots of
-// one 32-byte bucket together (one L2 sector); a ballot finds a matching key or
-// an empty slot.  Inserts claim the first empty slot with a 64-bit CAS.  Every
-// probe loop is bounded; exceeding the bound sets SPC_ERR_TABLE_FULL.
+// Buckets are 32 bytes (four slots, one L2 sector) and each lane reads a whole
+// bucket per step with two 16-byte loads, so one read resolves nearly every
+// lookup at load factor <= 1/2.  A warp works on 32 consecutive rows together:
+// their coordinates arrive in one coalesced read, their map entries leave as
+// 128-byte rows of imap, and the per-offset pair counts are one ballot per
+// offset.  Inserts claim the first empty slot with a 64-bit CAS.  Every probe
+// loop is bounded; exceeding the bound sets SPC_ERR_TABLE_FULL.
 #include "kernels.cuh"
 
 namespace spc {
@@ -40,180 +43,208 @@ k_hash_clear(unsigned long long* __restrict__ slots, int64_t n)
     for (; i < n / 2; i += stride) s2[i] = make_ulonglong2(EMPTY, EMPTY);
 }
 
-// One key per 4-lane group, eight per warp; the warp stays converged so the
-// ballots below always run with the full mask.
+// Reads one 32-byte bucket (four slots) with two 16-byte loads.
+template <bool COHERENT>
+__device__ __forceinline__ void load_bucket(const unsigned long long* slots, uint32_t bucket,
+                                            unsigned long long v[4])
+{
+    const ulonglong2* b = reinterpret_cast<const ulonglong2*>(slots + (size_t)bucket * 4);
+    ulonglong2 a, c;
+    if (COHERENT) {
+        a = __ldcg(b);
+        c = __ldcg(b + 1);
+    } else {
+        a = __ldg(b);
+        c = __ldg(b + 1);
+    }
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = c.x;
+    v[3] = c.y;
+}
+
+// One key per thread.  The thread reads its key's whole bucket at once; a slot
+// holding the same key means a duplicate row, else it claims the first empty
+// slot with a 64-bit CAS (re-reading the bucket if another thread won it), else
+// it moves to the next bucket.  Bounded by 5 visits per bucket of the table.
 __global__ void __launch_bounds__(kBlock)
 k_hash_insert(const int4* __restrict__ coords, int64_t n, int32_t batch, int D, int H, int W,
               unsigned long long* __restrict__ slots, int log2b, int vbits,
               int32_t* __restrict__ status)
 {
-    const int lane = threadIdx.x & 31, sub = lane & 3, gbase = lane & ~3;
     const uint32_t nb = 1u << log2b, nb_mask = nb - 1;
     const uint32_t bound = 5u * nb + 8u;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-
-    for (int64_t wb = warp * 8; wb < n; wb += nwarps * 8) {
-        const int64_t r = wb + (lane >> 2);
-        bool active = r < n;
-        unsigned long long key = 0;
-        if (active) {
-            const int4 c = coords[r];
-            if (c.x < 0 || c.x >= batch || c.y < 0 || c.y >= D || c.z < 0 || c.z >= H ||
-                c.w < 0 || c.w >= W) {
-                if (sub == 0) set_status(status, SPC_ERR_COORD_RANGE);
-                active = false;
-            } else {
-                key = cell_key(c.x, c.y, c.z, c.w, D, H, W);
-            }
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n;
+         r += (int64_t)gridDim.x * blockDim.x) {
+        const int4 c = coords[r];
+        if (c.x < 0 || c.x >= batch || c.y < 0 || c.y >= D || c.z < 0 || c.z >= H || c.w < 0 ||
+            c.w >= W) {
+            set_status(status, SPC_ERR_COORD_RANGE);
+            continue;
         }
+        const unsigned long long key = cell_key(c.x, c.y, c.z, c.w, D, H, W);
         const unsigned long long entry = (key << vbits) | (unsigned long long)r;
         uint32_t bucket = bucket_of(key, log2b);
-        for (uint32_t it = 0;; ++it) {
-            if (!__any_sync(FULL_MASK, active)) break;
-            if (it >= bound) {
-                if (active && sub == 0) set_status(status, SPC_ERR_TABLE_FULL);
+        uint32_t it = 0;
+        for (; it < bound; ++it) {
+            unsigned long long v[4];
+            load_bucket<true>(slots, bucket, v);
+            int empty = -1;
+            bool dup = false;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                dup |= v[q] != EMPTY && (v[q] >> vbits) == key;
+                if (empty < 0 && v[q] == EMPTY) empty = q;
+            }
+            if (dup) {
+                set_status(status, SPC_ERR_DUPLICATE);
                 break;
             }
-            // L2-coherent read: other warps fill slots while this one probes.
-            const unsigned long long s = active ? __ldcg(&slots[(size_t)bucket * 4 + sub]) : EMPTY;
-            const bool is_match = active && s != EMPTY && (s >> vbits) == key;
-            const bool is_empty = active && s == EMPTY;
-            const uint32_t gm = (__ballot_sync(FULL_MASK, is_match) >> gbase) & 0xFu;
-            const uint32_t ge = (__ballot_sync(FULL_MASK, is_empty) >> gbase) & 0xFu;
-            bool won = false;
-            if (active && gm == 0 && ge != 0 && sub == __ffs(ge) - 1) {
-                const unsigned long long old =
-                    atomicCAS(&slots[(size_t)bucket * 4 + sub], EMPTY, entry);
-                won = (old == EMPTY);
+            if (empty < 0) {
+                bucket = (bucket + 1) & nb_mask;
+                continue;
             }
-            const bool group_won = ((__ballot_sync(FULL_MASK, won) >> gbase) & 0xFu) != 0;
-            if (active) {
-                if (gm != 0) {
-                    if (sub == 0) set_status(status, SPC_ERR_DUPLICATE);
-                    active = false;
-                } else if (group_won) {
-                    active = false;
-                } else if (ge == 0) {
-                    bucket = (bucket + 1) & nb_mask;
-                }
-                // else: another group took the slot first; read the bucket again
+            const unsigned long long old =
+                atomicCAS(&slots[(size_t)bucket * 4 + empty], EMPTY, entry);
+            if (old == EMPTY) break;
+            if ((old >> vbits) == key) {
+                set_status(status, SPC_ERR_DUPLICATE);
+                break;
             }
+            // another key took that slot first: read the same bucket again
         }
+        if (it >= bound) set_status(status, SPC_ERR_TABLE_FULL);
     }
 }
 
-// Probe: for each query row r and offset k, the input row at the offset cell.
-// ILP: the first bucket of U offsets is loaded before any of them is resolved.
-template <bool WRITE_T>
+// Row of `key`, or -1: resolves the bucket already read in `v`, then walks on.
+__device__ __forceinline__ int32_t finish_lookup(const unsigned long long* __restrict__ slots,
+                                                 unsigned long long key, uint32_t bucket,
+                                                 unsigned long long v[4], int log2b, int vbits,
+                                                 int32_t* __restrict__ status)
+{
+    const unsigned long long vmask = (1ull << vbits) - 1;
+    const uint32_t nb = 1u << log2b, nb_mask = nb - 1;
+    for (uint32_t it = 0;; ++it) {
+        bool empty = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (v[q] != EMPTY && (v[q] >> vbits) == key) return (int32_t)(v[q] & vmask);
+            empty |= v[q] == EMPTY;
+        }
+        if (empty) return -1;
+        if (it + 1 >= nb) {
+            set_status(status, SPC_ERR_TABLE_FULL);
+            return -1;
+        }
+        bucket = (bucket + 1) & nb_mask;
+        load_bucket<false>(slots, bucket, v);
+    }
+}
+
+// Probe.  A thread owns one output row and a group of kGroup consecutive
+// offsets of the probe list; blockIdx.y picks the group, so a warp holds 32
+// consecutive rows of one group: coordinates arrive coalesced, map entries
+// leave as 128-byte rows of imap, and the group's first buckets are all in
+// flight before any is resolved.
+//
+// MIRROR (submanifold maps): offset k and K-1-k are mirror images (d and -d),
+// so imap[K-1-k, i] = o exactly when imap[k, o] = i.  Only k < centre is
+// probed; a hit also writes its mirror entry and mirror mask bit, the centre is
+// the identity, and the caller has filled imap rows k > centre with -1 and the
+// mask with 0 beforehand.
+constexpr int kGroup = 3;
+
+template <bool WRITE_T, bool MIRROR>
 __global__ void __launch_bounds__(kBlock)
-k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g,
+k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, int n_probe,
             const unsigned long long* __restrict__ slots, int log2b, int vbits,
             int32_t* __restrict__ imap, int32_t* __restrict__ imap_t,
             int32_t* __restrict__ pair_count, uint32_t* __restrict__ mask,
             int32_t* __restrict__ status)
 {
-    constexpr int U = 9;
-    extern __shared__ int32_t s_cnt[];  // [K]
-    const int lane = threadIdx.x & 31, sub = lane & 3, gbase = lane & ~3;
-    const uint32_t nb = 1u << log2b, nb_mask = nb - 1;
-    const unsigned long long vmask = (1ull << vbits) - 1;
+    __shared__ int32_t s_cnt[kGroup];
+    const int lane = threadIdx.x & 31;
     const int K = g.K;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) s_cnt[k] = 0;
+    const int k0 = blockIdx.y * kGroup;
+    if (threadIdx.x < kGroup) s_cnt[threadIdx.x] = 0;
     __syncthreads();
-
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int D = g.in_shape[0], H = g.in_shape[1], W = g.in_shape[2];
+    const int kyx = g.ksize[1] * g.ksize[2];
 
-    for (int64_t wb = warp * 8; wb < nq; wb += nwarps * 8) {
-        const int64_t r = wb + (lane >> 2);
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < nq;
+         base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = base + threadIdx.x;
         bool valid = r < nq;
         int4 c = make_int4(0, 0, 0, 0);
         if (valid) {
             c = q[r];
             if (c.x < 0 || c.x >= g.batch || c.y < 0 || c.y >= g.q_shape[0] || c.z < 0 ||
                 c.z >= g.q_shape[1] || c.w < 0 || c.w >= g.q_shape[2]) {
-                if (sub == 0) set_status(status, SPC_ERR_COORD_RANGE);
+                if (blockIdx.y == 0) set_status(status, SPC_ERR_COORD_RANGE);
                 valid = false;
             }
         }
         const int bz = c.y * g.stride[0] - g.pad[0];
         const int by = c.z * g.stride[1] - g.pad[1];
         const int bx = c.w * g.stride[2] - g.pad[2];
-        uint32_t m = 0;
 
-        for (int k0 = 0; k0 < K; k0 += U) {
-            unsigned long long key[U], s[U];
-            uint32_t bucket[U];
-            bool act[U];
+        unsigned long long key[kGroup], v[kGroup][4];
+        uint32_t bucket[kGroup];
+        bool act[kGroup];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = k0 + u;
-                act[u] = false;
-                key[u] = 0;
-                bucket[u] = 0;
-                s[u] = EMPTY;
-                if (k < K && valid && k != g.centre) {
-                    const int kx = k % g.ksize[2];
-                    const int ky = (k / g.ksize[2]) % g.ksize[1];
-                    const int kz = k / (g.ksize[2] * g.ksize[1]);
-                    const int z = bz + kz * g.dil[0], y = by + ky * g.dil[1], x = bx + kx * g.dil[2];
-                    if (z >= 0 && z < D && y >= 0 && y < H && x >= 0 && x < W) {
-                        act[u] = true;
-                        key[u] = cell_key(c.x, z, y, x, D, H, W);
-                        bucket[u] = bucket_of(key[u], log2b);
-                        s[u] = __ldg(&slots[(size_t)bucket[u] * 4 + sub]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = k0 + u;
-                if (k >= K) break;  // warp-uniform
-                int32_t row = -1;
-                bool active = act[u];
-                unsigned long long sv = s[u];
-                for (uint32_t it = 0;; ++it) {
-                    const bool is_match = active && sv != EMPTY && (sv >> vbits) == key[u];
-                    const bool is_empty = active && sv == EMPTY;
-                    const uint32_t bm = __ballot_sync(FULL_MASK, is_match);
-                    const uint32_t be = __ballot_sync(FULL_MASK, is_empty);
-                    const uint32_t gm = (bm >> gbase) & 0xFu, ge = (be >> gbase) & 0xFu;
-                    const int src = gm ? gbase + __ffs(gm) - 1 : lane;
-                    const unsigned long long hit = __shfl_sync(FULL_MASK, sv, src);
-                    if (active) {
-                        if (gm) {
-                            row = (int32_t)(hit & vmask);
-                            active = false;
-                        } else if (ge) {
-                            active = false;
-                        } else if (it + 1 >= nb) {
-                            if (sub == 0) set_status(status, SPC_ERR_TABLE_FULL);
-                            active = false;
-                        } else {
-                            bucket[u] = (bucket[u] + 1) & nb_mask;
-                        }
-                    }
-                    if (!__any_sync(FULL_MASK, active)) break;
-                    sv = active ? __ldg(&slots[(size_t)bucket[u] * 4 + sub]) : EMPTY;
-                }
-                if (valid && k == g.centre) row = (int32_t)r;
-                const bool hitb = row >= 0;
-                if (sub == 0 && valid) {
-                    imap[(int64_t)k * nq + r] = row;
-                    if (WRITE_T && hitb) imap_t[(int64_t)k * n_in + row] = (int32_t)r;
-                }
-                m |= (hitb ? 1u : 0u) << (k & 31);
-                const uint32_t hits = __popc(__ballot_sync(FULL_MASK, sub == 0 && hitb));
-                if (lane == 0 && hits) atomicAdd(&s_cnt[k], (int32_t)hits);
-            }
+        for (int u = 0; u < kGroup; ++u) {
+            const int k = k0 + u;
+            const int kz = k / kyx, ky = (k / g.ksize[2]) % g.ksize[1], kx = k % g.ksize[2];
+            const int z = bz + kz * g.dil[0], y = by + ky * g.dil[1], x = bx + kx * g.dil[2];
+            act[u] = valid && k < n_probe && k != g.centre && z >= 0 && z < D && y >= 0 &&
+                     y < H && x >= 0 && x < W;
+            key[u] = act[u] ? cell_key(c.x, z, y, x, D, H, W) : 0ull;
+            bucket[u] = bucket_of(key[u], log2b);
+            if (act[u]) load_bucket<false>(slots, bucket[u], v[u]);
         }
-        if (mask && sub == 0 && valid) mask[r] = m;
+        uint32_t bits = 0;
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u) {
+            const int k = k0 + u;
+            if (k >= n_probe) break;  // block-uniform
+            int32_t row = -1;
+            if (act[u]) row = finish_lookup(slots, key[u], bucket[u], v[u], log2b, vbits, status);
+            if (valid && k == g.centre) row = (int32_t)r;
+            const bool hit = row >= 0;
+            if (valid) {
+                imap[(int64_t)k * nq + r] = row;
+                if (WRITE_T && hit) imap_t[(int64_t)k * n_in + row] = (int32_t)r;
+                if (MIRROR && hit && k != g.centre) {
+                    imap[(int64_t)(K - 1 - k) * nq + row] = (int32_t)r;
+                    if (mask) atomicOr(&mask[row], 1u << ((K - 1 - k) & 31));
+                }
+            }
+            bits |= (hit ? 1u : 0u) << (k & 31);
+            const uint32_t hits = __popc(__ballot_sync(FULL_MASK, hit));
+            if (lane == 0 && hits) atomicAdd(&s_cnt[u], (int32_t)hits);
+        }
+        if (mask && valid && bits) atomicOr(&mask[r], bits);
     }
     __syncthreads();
-    for (int k = threadIdx.x; k < K; k += blockDim.x)
-        if (s_cnt[k]) atomicAdd(&pair_count[k], s_cnt[k]);
+    if (threadIdx.x < kGroup) {
+        const int k = k0 + threadIdx.x;
+        const int32_t n = s_cnt[threadIdx.x];
+        if (k < n_probe && n) {
+            atomicAdd(&pair_count[k], n);
+            if (MIRROR && k != g.centre) atomicAdd(&pair_count[K - 1 - k], n);
+        }
+    }
+}
+
+template <bool WRITE_T, bool MIRROR>
+void launch_probe(dim3 grid, cudaStream_t st, const int32_t* qcoords, int64_t nq, int64_t n_in,
+                  const ProbeGeom& g, int n_probe, HashTable t, int32_t* imap, int32_t* imap_t,
+                  int32_t* pair_count, uint32_t* mask, int32_t* status)
+{
+    k_map_probe<WRITE_T, MIRROR><<<grid, kBlock, 0, st>>>(
+        reinterpret_cast<const int4*>(qcoords), nq, n_in, g, n_probe, t.slots, t.log2_buckets,
+        t.vbits, imap, imap_t, pair_count, mask, status);
 }
 
 }  // namespace
@@ -251,8 +282,7 @@ spc_status hash_insert(const int32_t* coords, int64_t n, int32_t batch, const in
                        HashTable t, int32_t* status, cudaStream_t st)
 {
     if (n == 0) return SPC_OK;
-    const int64_t warps = ceil_div(n, 8);
-    const int grid = (int)std::min<int64_t>(ceil_div(warps * 32, kBlock), 16 * sm_count());
+    const int grid = (int)std::min<int64_t>(ceil_div(n, kBlock), 8 * sm_count());
     k_hash_insert<<<grid, kBlock, 0, st>>>(reinterpret_cast<const int4*>(coords), n, batch,
                                            shape[0], shape[1], shape[2], t.slots,
                                            t.log2_buckets, t.vbits, status);
@@ -265,18 +295,20 @@ spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const Pro
                      uint32_t* mask, int32_t* status, cudaStream_t st)
 {
     if (nq == 0) return SPC_OK;
-    const int64_t warps = ceil_div(nq, 8);
-    const int grid = (int)std::min<int64_t>(ceil_div(warps * 32, kBlock), 16 * sm_count());
-    const size_t smem = sizeof(int32_t) * (size_t)g.K;
-    if (imap_t) {
-        k_map_probe<true><<<grid, kBlock, smem, st>>>(
-            reinterpret_cast<const int4*>(qcoords), nq, n_in, g, t.slots, t.log2_buckets, t.vbits,
-            imap, imap_t, pair_count, mask, status);
-    } else {
-        k_map_probe<false><<<grid, kBlock, smem, st>>>(
-            reinterpret_cast<const int4*>(qcoords), nq, n_in, g, t.slots, t.log2_buckets, t.vbits,
-            imap, nullptr, pair_count, mask, status);
-    }
+    // submanifold maps (centre >= 0, odd kernels) are probed for k <= centre only
+    const bool mirror = g.centre >= 0 && imap_t == nullptr && g.K == 2 * g.centre + 1;
+    const int n_probe = mirror ? g.centre + 1 : g.K;
+    if (mask) SPC_CUDA_TRY(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * (size_t)nq, st));
+    if (mirror && g.K > n_probe)
+        SPC_CUDA_TRY(cudaMemsetAsync(imap + (int64_t)n_probe * nq, 0xFF,
+                                     sizeof(int32_t) * (size_t)(g.K - n_probe) * (size_t)nq, st));
+    const int groups = (int)ceil_div(n_probe, kGroup);
+    const int64_t row_blocks = ceil_div(nq, kBlock);
+    const int64_t cap = std::max<int64_t>(1, (int64_t)16 * sm_count() / groups);
+    dim3 grid((unsigned)std::min<int64_t>(row_blocks, cap), (unsigned)groups);
+    if (imap_t) launch_probe<true, false>(grid, st, qcoords, nq, n_in, g, n_probe, t, imap, imap_t, pair_count, mask, status);
+    else if (mirror) launch_probe<false, true>(grid, st, qcoords, nq, n_in, g, n_probe, t, imap, nullptr, pair_count, mask, status);
+    else launch_probe<false, false>(grid, st, qcoords, nq, n_in, g, n_probe, t, imap, nullptr, pair_count, mask, status);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }

@@ -78,6 +78,10 @@ struct GatherGemm {
 };
 spc_status conv_gather_simt(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
 
+// Narrow channels (cred, cout in {8, 16, 32}): one thread per output row.
+bool conv_narrow_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt);
+spc_status conv_gather_narrow(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
+
 // dW[k] = sum_o x[map[k,o]]^T dy[o] in fp32, deterministic split over output rows.
 struct WgradArgs {
     const void* x;

@@ -113,7 +113,11 @@ def test_argument_errors_return_before_any_work(L):
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(258), None, ctypes.c_void_p(256),
                           None, 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, 0, None) == E
     assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
-                            binding.SPC_MAP_SUBM_MIRROR, 27, 4, 5, 8, 8, 0, 0,
+                            binding.SPC_MAP_SUBM_MIRROR, None, 27, 4, 5, 8, 8, 0, 0,
+                            ctypes.c_void_p(256), None, 0, None) == E
+    # a mask is only accepted with a submanifold map
+    assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
+                            binding.SPC_MAP_TRANSPOSED, ctypes.c_void_p(256), 27, 4, 4, 8, 8, 0, 0,
                             ctypes.c_void_p(256), None, 0, None) == E
     assert L.spc_conv_wgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), 27,
                             4, 4, 8, 8, 2, 0, ctypes.c_void_p(256), None, 0, None) == 8

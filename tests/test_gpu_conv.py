@@ -45,7 +45,8 @@ def subm_case(coords, batch, shape, cin, cout, dtype, ks=3, seed=0, bias=True):
 @pytest.mark.parametrize("dtype,prec", [("f32", "exact"), ("f32", "tf32"), ("f16", "exact"),
                                         ("bf16", "exact")])
 @pytest.mark.parametrize("n,cin,cout", [(1, 8, 8), (777, 16, 16), (1500, 24, 40),
-                                        (2100, 64, 128), (900, 128, 96)])
+                                        (2100, 64, 128), (900, 128, 96), (640, 32, 32),
+                                        (333, 16, 32), (1029, 32, 16), (515, 8, 16)])
 def test_subm_small_full(dtype, prec, n, cin, cout):
     g = np.random.default_rng(n)
     batch, shape = 2, (12, 11, 13)
@@ -54,10 +55,17 @@ def test_subm_small_full(dtype, prec, n, cin, cout):
     p = spc.SPC_PREC_TF32 if prec == "tf32" else spc.SPC_PREC_EXACT
     d = dev()
     tol = TOL[(dtype, prec)]
+    y_ref = oracle.conv_fwd(x, w, b, imap_ref)
     y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], m["mask"], precision=p)
-    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, imap_ref)) < tol
+    assert normwise(to_np(y), y_ref) < tol
+    y_nomask = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], None, precision=p)
+    assert normwise(to_np(y_nomask), y_ref) < tol
+    dx_ref = oracle.conv_dgrad(dy, w, imap_ref, n)
     dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, precision=p)
-    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, n)) < tol
+    assert normwise(to_np(dx), dx_ref) < tol
+    dxm = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, precision=p,
+                             mask=m["mask"])
+    assert normwise(to_np(dxm), dx_ref) < tol
     dw = spc.spc_conv_wgrad(x.to(d), dy.to(d), m["imap"], 27, precision=p)
     assert normwise(to_np(dw), oracle.conv_wgrad(x, dy, imap_ref)) < tol
 
@@ -151,7 +159,7 @@ def test_training_step_shell192x4_sampled():
     imap_ref, _ = oracle.subm_map(c, 4, (192, 192, 192))
     x, wt, dy = w["x"].to(d), w["w"].to(d), w["dy"].to(d)
     y = spc.spc_conv_fwd(x, wt, None, m["imap"], m["mask"])
-    dx = spc.spc_conv_dgrad(dy, wt, m["imap"], spc.SPC_MAP_SUBM_MIRROR, n)
+    dx = spc.spc_conv_dgrad(dy, wt, m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, mask=m["mask"])
     dw = spc.spc_conv_wgrad(x, dy, m["imap"], 27)
     rows = sample_rows(n, seed=1)
     r = torch.from_numpy(rows).to(d)
@@ -163,7 +171,7 @@ def test_training_step_shell192x4_sampled():
     ref = oracle.conv_wgrad_entries(w["x"], w["dy"], imap_ref, ent)
     assert normwise(to_np(dw).reshape(-1)[ent], ref) < 2e-2
     dw2 = spc.spc_conv_wgrad(x, dy, m["imap"], 27)
-    dx2 = spc.spc_conv_dgrad(dy, wt, m["imap"], spc.SPC_MAP_SUBM_MIRROR, n)
+    dx2 = spc.spc_conv_dgrad(dy, wt, m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, mask=m["mask"])
     assert torch.equal(dw, dw2) and torch.equal(dx, dx2)
 
 
