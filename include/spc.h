@@ -66,7 +66,8 @@ typedef enum {
     SPC_ERR_CAPACITY = 5,      /* the strided output set exceeds the caller's buffer */
     SPC_ERR_UNSUPPORTED = 6,   /* a valid request this build does not implement */
     SPC_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch, copy) */
-    SPC_ERR_WORKSPACE = 8      /* workspace missing or smaller than required */
+    SPC_ERR_WORKSPACE = 8,     /* workspace missing or smaller than required */
+    SPC_ERR_TIMEOUT = 9        /* an internal GPU wait exceeded its bound (2 s); results invalid */
 } spc_status;
 
 typedef enum { SPC_F32 = 0, SPC_F16 = 1, SPC_BF16 = 2 } spc_dtype;
@@ -215,16 +216,23 @@ SPC_API spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, i
  *  mask  [n_out] uint32 or NULL: the per-row offset mask from
  *        spc_build_indice_map; lets tiles skip offsets no row of theirs uses.
  *  y     [n_out, cout] of dtype dt out (fp32 accumulate, one rounding).
- *  ws    spc_conv_workspace_size(...) bytes.
+ *  status  device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
+ *  ws    spc_conv_workspace_size(...) bytes (the tensor-core path keeps the
+ *        weights transposed to [K, Cout, Cin] there).
  *  x, w, y must be 16-byte aligned.
+ *  Kernels: tcgen05 tensor cores when the channels allow (fp16 / bf16 with
+ *  Cin % 64 == 0, or fp32 with SPC_PREC_TF32 and Cin % 32 == 0; Cout % 64 ==
+ *  0; K <= 32), a one-row-per-thread kernel for narrow channels (Cin, Cout in
+ *  {8, 16, 32}), else a tiled CUDA-core kernel.
  */
 SPC_API size_t spc_conv_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
                                int32_t cout, spc_dtype dt);
 
-SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
-                        const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
-                        int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec, void* y,
-                        void* ws, size_t ws_bytes, void* stream);
+SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias,
+                                const int32_t* imap, const uint32_t* mask, int32_t K,
+                                int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
+                                spc_dtype dt, spc_precision prec, void* y, int32_t* status,
+                                void* ws, size_t ws_bytes, void* stream);
 
 /* spc_conv_dgrad -- dx[i, :] = sum over pairs imap[k, o] = i of W[k] dy[o, :]
  * (the gradient of spc_conv_fwd with respect to x; "dinput" in the HYGON-AI
@@ -239,12 +247,15 @@ SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, 
  *        spc_build_indice_map wrote for that submanifold map (the kernel
  *        mirrors its bits itself).
  *  dx    [n_in, cin] of dtype dt out.
+ *  status  device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
+ *  Kernels as for spc_conv_fwd with the roles of Cin and Cout exchanged; no
+ *  workspace is needed.
  */
 SPC_API spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map,
                                   spc_map_kind kind, const uint32_t* mask, int32_t K, int64_t n_in,
                                   int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
-                                  spc_precision prec, void* dx, void* ws, size_t ws_bytes,
-                                  void* stream);
+                                  spc_precision prec, void* dx, int32_t* status, void* ws,
+                                  size_t ws_bytes, void* stream);
 
 /* spc_conv_wgrad -- dW[k] = sum_{o: imap[k, o] = i != -1} x[i, :]^T dy[o, :],
  * reduced in fp32 over all active pairs ("dfilter" in the HYGON-AI spconv-das

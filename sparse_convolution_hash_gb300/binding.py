@@ -24,7 +24,7 @@ SPC_OK = 0
 STATUS_NAMES = {
     0: "SPC_OK", 1: "SPC_ERR_INVALID_ARG", 2: "SPC_ERR_COORD_RANGE", 3: "SPC_ERR_DUPLICATE",
     4: "SPC_ERR_TABLE_FULL", 5: "SPC_ERR_CAPACITY", 6: "SPC_ERR_UNSUPPORTED", 7: "SPC_ERR_CUDA",
-    8: "SPC_ERR_WORKSPACE",
+    8: "SPC_ERR_WORKSPACE", 9: "SPC_ERR_TIMEOUT",
 }
 SPC_F32, SPC_F16, SPC_BF16 = 0, 1, 2
 SPC_PREC_EXACT, SPC_PREC_TF32 = 0, 1
@@ -105,10 +105,10 @@ def lib():
             L.spc_conv_workspace_size.argtypes = [_i32, _i64, _i64, _i32, _i32, _i32]
             L.spc_conv_workspace_size.restype = _sz
             L.spc_conv_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
-                                       _i32, _p, _p, _sz, _p]
+                                       _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd.restype = _i32
             L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _i32, _i64, _i64, _i32, _i32,
-                                         _i32, _i32, _p, _p, _sz, _p]
+                                         _i32, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_dgrad.restype = _i32
             L.spc_conv_wgrad_workspace_size.argtypes = [_i32, _i64, _i64, _i32, _i32, _i32]
             L.spc_conv_wgrad_workspace_size.restype = _sz
@@ -248,8 +248,12 @@ def spc_strided_out_coords(coords: torch.Tensor, batch: int, in_shape, ksize=3, 
 def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
                  imap: Optional[torch.Tensor], mask: Optional[torch.Tensor] = None,
                  n_out: Optional[int] = None, precision: int = SPC_PREC_EXACT,
-                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """y[o] = bias + sum over pairs of x[imap[k, o]] W[k]; y has x's dtype."""
+                 out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                 ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y[o] = bias + sum over pairs of x[imap[k, o]] W[k]; y has x's dtype.
+
+    Pass `out`, `ws` (spc_conv_workspace_size bytes) and `status` to call
+    without allocating (e.g. inside CUDA-graph capture)."""
     x = _cuda(x, "x")
     w = _cuda(w, "w").to(x.dtype)
     b = _cuda(bias, "bias").to(x.dtype) if bias is not None else None
@@ -262,9 +266,10 @@ def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
     y = torch.empty((n_out, cout), dtype=x.dtype, device=x.device) if out is None else out
     dt = _DTYPES[x.dtype]
     nbytes = int(lib().spc_conv_workspace_size(K, x.shape[0], n_out, cin, cout, dt))
-    ws = _workspace(nbytes, x.device) if nbytes else None
+    if nbytes and (ws is None or ws.numel() < nbytes):
+        ws = _workspace(nbytes, x.device)
     code = lib().spc_conv_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(imap), _ptr(mask), K, x.shape[0],
-                              n_out, cin, cout, dt, precision, _ptr(y), _ptr(ws),
+                              n_out, cin, cout, dt, precision, _ptr(y), _ptr(status), _ptr(ws),
                               0 if ws is None else ws.numel(), _stream(x.device))
     _check(code, "spc_conv_fwd")
     return y
@@ -272,7 +277,8 @@ def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
 
 def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tensor], kind: int,
                    n_in: int, precision: int = SPC_PREC_EXACT, mask: Optional[torch.Tensor] = None,
-                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                   out: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None) -> torch.Tensor:
     """dx[i] = sum over pairs imap[k, o] = i of W[k] dy[o]."""
     dy = _cuda(dy, "dy")
     w = _cuda(w, "w").to(dy.dtype)
@@ -281,8 +287,8 @@ def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tenso
     dx = torch.empty((n_in, cin), dtype=dy.dtype, device=dy.device) if out is None else out
     dt = _DTYPES[dy.dtype]
     code = lib().spc_conv_dgrad(_ptr(dy), _ptr(w), _ptr(m), kind, _ptr(mask), K, n_in,
-                                dy.shape[0], cin, cout, dt, precision, _ptr(dx), None, 0,
-                                _stream(dy.device))
+                                dy.shape[0], cin, cout, dt, precision, _ptr(dx), _ptr(status),
+                                None, 0, _stream(dy.device))
     _check(code, "spc_conv_dgrad")
     return dx
 

@@ -55,6 +55,7 @@ const char* spc_status_string(spc_status s)
     case SPC_ERR_UNSUPPORTED: return "unsupported configuration";
     case SPC_ERR_CUDA: return "CUDA runtime error";
     case SPC_ERR_WORKSPACE: return "workspace missing or too small";
+    case SPC_ERR_TIMEOUT: return "an internal GPU wait exceeded its bound";
     }
     return "unknown status";
 }
@@ -186,12 +187,12 @@ spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, int32_t b
 size_t spc_conv_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
                                spc_dtype dt)
 {
-    (void)K;
     (void)n_in;
     (void)n_out;
-    (void)cin;
-    (void)cout;
-    (void)dt;
+    if (K < 1 || cin < 1 || cout < 1 || !dtype_ok(dt)) return 0;
+    if (conv_tc_supported(cin, cout, K, dt, SPC_PREC_EXACT) ||
+        conv_tc_supported(cin, cout, K, dt, SPC_PREC_TF32))
+        return conv_tc_weight_bytes(K, cin, cout, dt);
     return 0;
 }
 
@@ -210,8 +211,8 @@ spc_status check_conv(const void* a, const void* w, const void* out, int32_t K, 
     return SPC_OK;
 }
 
-// Picks the conv kernel for a gathered GEMM: the narrow-channel kernel when the
-// channel widths allow it, else the general tiled CUDA-core kernel.
+// Picks the conv kernel for a gathered GEMM on CUDA cores: the narrow-channel
+// kernel when the channel widths allow it, else the general tiled kernel.
 spc_status run_gather(const GatherGemm& p, spc_dtype dt, cudaStream_t st)
 {
     if (conv_narrow_supported(p.cred, p.cout, p.K, dt) && aligned16(p.in) && aligned16(p.out)) {
@@ -225,11 +226,9 @@ spc_status run_gather(const GatherGemm& p, spc_dtype dt, cudaStream_t st)
 
 spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
                         const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
-                        int32_t cout, spc_dtype dt, spc_precision prec, void* y, void* ws,
-                        size_t ws_bytes, void* stream)
+                        int32_t cout, spc_dtype dt, spc_precision prec, void* y, int32_t* status,
+                        void* ws, size_t ws_bytes, void* stream)
 {
-    (void)ws;
-    (void)ws_bytes;
     spc_status s = check_conv(x, w, y, K, n_in, n_out, cin, cout, dt);
     if (s != SPC_OK) return s;
     if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
@@ -249,13 +248,36 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
     p.cout = cout;
     p.mirror = 0;
     p.transpose_w = 0;
-    return run_gather(p, dt, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_out > 0 && conv_tc_supported(cin, cout, K, dt, prec) && aligned16(x) && aligned16(y)) {
+        const size_t wbytes = conv_tc_weight_bytes(K, cin, cout, dt);
+        if (!ws || ws_bytes < wbytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+            return SPC_ERR_WORKSPACE;
+        s = transpose_weights(w, ws, K, cin, cout, dt, st);
+        if (s != SPC_OK) return s;
+        TcArgs a;
+        a.in = x;
+        a.b = ws;
+        a.bias = bias;
+        a.map = imap;
+        a.mask = mask;
+        a.out = y;
+        a.status = status;
+        a.rows = n_out;
+        a.in_rows = n_in;
+        a.K = K;
+        a.cred = cin;
+        a.n_total = cout;
+        a.mirror = 0;
+        return conv_gather_tc(a, dt, st);
+    }
+    return run_gather(p, dt, st);
 }
 
 spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
                           const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
                           int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec, void* dx,
-                          void* ws, size_t ws_bytes, void* stream)
+                          int32_t* status, void* ws, size_t ws_bytes, void* stream)
 {
     (void)ws;
     (void)ws_bytes;
@@ -280,7 +302,26 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     p.cout = cin;
     p.mirror = (kind == SPC_MAP_SUBM_MIRROR) ? 1 : 0;
     p.transpose_w = 1;
-    return run_gather(p, dt, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_in > 0 && conv_tc_supported(cout, cin, K, dt, prec) && aligned16(dy) && aligned16(dx)) {
+        // W[k] is [Cin][Cout]: already the [N][K] K-major operand of dx = dy W[k]^T
+        TcArgs a;
+        a.in = dy;
+        a.b = w;
+        a.bias = nullptr;
+        a.map = map;
+        a.mask = mask;
+        a.out = dx;
+        a.status = status;
+        a.rows = n_in;
+        a.in_rows = n_out;
+        a.K = K;
+        a.cred = cout;
+        a.n_total = cin;
+        a.mirror = p.mirror;
+        return conv_gather_tc(a, dt, st);
+    }
+    return run_gather(p, dt, st);
 }
 
 size_t spc_conv_wgrad_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,

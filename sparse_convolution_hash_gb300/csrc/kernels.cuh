@@ -82,6 +82,25 @@ spc_status conv_gather_simt(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
 bool conv_narrow_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt);
 spc_status conv_gather_narrow(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
 
+// Tensor-core gathered GEMM (tcgen05): out[r, n] = bias[n] + sum_k sum_c
+// in[map(k, r), c] * b[k][n][c], with b already in [K][n_total][cred] order.
+struct TcArgs {
+    const void* in;
+    const void* b;
+    const void* bias;
+    const int32_t* map;
+    const uint32_t* mask;
+    void* out;
+    int32_t* status;
+    int64_t rows, in_rows;
+    int32_t K, cred, n_total, mirror;
+};
+bool conv_tc_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt, spc_precision prec);
+size_t conv_tc_weight_bytes(int32_t K, int32_t cin, int32_t cout, spc_dtype dt);
+spc_status transpose_weights(const void* w, void* wt, int32_t K, int32_t cin, int32_t cout,
+                             spc_dtype dt, cudaStream_t st);
+spc_status conv_gather_tc(const TcArgs& a, spc_dtype dt, cudaStream_t st);
+
 // dW[k] = sum_o x[map[k,o]]^T dy[o] in fp32, deterministic split over output rows.
 struct WgradArgs {
     const void* x;

@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_status_strings_and_version(L):
     assert binding.spc_version() >= 100
-    for code in range(9):
+    for code in range(10):
         assert binding.spc_status_string(code)
     assert binding.spc_status_string(99) == "unknown status"
 
@@ -107,18 +107,24 @@ def test_argument_errors_return_before_any_work(L):
                                   None) == E
     # conv: bad dtype, missing map for K > 1, misaligned weight
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, None, 27, 4, 4,
-                          8, 8, 7, 0, ctypes.c_void_p(256), None, 0, None) == E
+                          8, 8, 7, 0, ctypes.c_void_p(256), None, None, 0, None) == E
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, None, 27, 4, 4,
-                          8, 8, 0, 0, ctypes.c_void_p(256), None, 0, None) == E
+                          8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0, None) == E
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(258), None, ctypes.c_void_p(256),
-                          None, 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, 0, None) == E
+                          None, 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0,
+                          None) == E
+    # the tensor-core path needs its workspace (transposed weights)
+    assert L.spc_conv_workspace_size(27, 4, 4, 128, 128, binding.SPC_BF16) == 27 * 128 * 128 * 2
+    assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256),
+                          None, 27, 4, 4, 128, 128, binding.SPC_BF16, 0, ctypes.c_void_p(256),
+                          None, None, 0, None) == 8
     assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
                             binding.SPC_MAP_SUBM_MIRROR, None, 27, 4, 5, 8, 8, 0, 0,
-                            ctypes.c_void_p(256), None, 0, None) == E
+                            ctypes.c_void_p(256), None, None, 0, None) == E
     # a mask is only accepted with a submanifold map
     assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
                             binding.SPC_MAP_TRANSPOSED, ctypes.c_void_p(256), 27, 4, 4, 8, 8, 0, 0,
-                            ctypes.c_void_p(256), None, 0, None) == E
+                            ctypes.c_void_p(256), None, None, 0, None) == E
     assert L.spc_conv_wgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), 27,
                             4, 4, 8, 8, 2, 0, ctypes.c_void_p(256), None, 0, None) == 8
     # strided out coords: null n_out / status
