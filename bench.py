@@ -1,19 +1,26 @@
 """Benchmark of the sparse-convolution hot path on one or more GPUs.
 
-One step = one pass of the submanifold path over the LiDAR-like scene (batch 2,
-41 x 1600 x 1408 grid, 120,000 voxels, fp16 features 16 -> 16):
-  spc_build_indice_map (validate + key + hash build + probe of all 27 offsets),
-  then spc_conv_fwd over the map.
-The headline value is conv TFLOP/s over active pairs (2 * P * Cin * Cout per
-step) divided by the whole step time; the indice-map rate (Mvoxel/s) and the
-conv-only rate are reported beside it.  Inputs are resident in HBM when the
-timed region starts; L2 is flushed (256 MiB write) between timed steps,
-outside the timed events.  `e2e` times the same step through the C ABI from
-pinned host buffers, host->device copies of the inputs and the device->host
-copy of the output inside the timed region.
+Default workload (one JSON line): the LiDAR-like scene, batch 2, 41 x 1600 x
+1408 grid, 120,000 voxels, fp16 features 16 -> 16.  One step = one pass of
+its hot path: spc_build_indice_map (validate + key + hash build + probe of all
+27 offsets) then spc_conv_fwd over the map.  The headline value is conv
+TFLOP/s over active pairs (2 * P * Cin * Cout per step) over the whole step
+time; the indice-map rate (Mvoxel/s) and per-phase times are reported beside
+it.  Other workloads (--workload) cover the remaining rows of the path: the
+strided k3 s2 p1 conv (output coordinates + maps + forward), the 256^3 shell
+at 128 -> 128 (k3 and k1), and the 4 x 192^3 training step (forward, dinput,
+dfilter).
 
---impl reference runs the CPU oracle (the slow fp64 restatement of the method
-used by the tests) on the host cores, on a bounded sample of the same workload.
+Timing: every phase is captured once as a CUDA graph (the C ABI allocates
+nothing and only enqueues on the current stream) and replayed; CUDA events on
+the launching stream bracket each phase.  Inputs are resident in HBM when the
+timed region starts and L2 is flushed (256 MiB write) between timed steps,
+outside the events.  `e2e` times the calls a user makes through the C ABI from
+pinned host buffers, with the host->device copies of the inputs and the
+device->host copies of the outputs inside the timed region.
+
+--impl reference times the CPU oracle (the slow fp64 restatement of the
+method the tests check against) on the host cores, on a bounded sample.
 
 Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
 the workload (voxels of different scenes never interact, so the path shards by
@@ -23,6 +30,7 @@ scene with no data exchange); value = work of all ranks / max time over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -39,12 +47,22 @@ sys.path.insert(0, ROOT)
 import scenes  # noqa: E402
 
 METRIC = "SubM3d conv TFLOP/s over active pairs (and % roofline); indice-map Mvoxel/s"
-WORKLOAD = "lidar_subm_f16"
-SHAPE = (41, 1600, 1408)
-BATCH = 2
+DEFAULT_WORKLOAD = "lidar_subm_f16"
 L2_FLUSH_BYTES = 256 << 20
-# kernels of ours per step: build = hash clear + insert + probe; fwd = 1
-LAUNCHES_PER_STEP = 4
+SHAPES = {"uniform32": (32, 32, 32), "lidar": (41, 1600, 1408), "shell256": (256, 256, 256),
+          "shell192x4": (192, 192, 192)}
+DESCRIPTIONS = {
+    "lidar_subm_f16": "SubMConv3d k3 indice build + forward, batch 2, 41x1600x1408 grid, "
+                      "120000 voxels, fp16 16->16, no bias",
+    "uniform32_subm_f32": "SubMConv3d k3 indice build + forward, 2000 voxels of 32^3, fp32 16->16, bias",
+    "uniform32_strided_bf16": "SparseConv3d k3 s2 p1 output coords + maps + forward, 2000 voxels "
+                              "of 32^3, bf16 64->128",
+    "shell256_subm_bf16": "SubMConv3d k3 indice build + forward, 256^3 shell, bf16 128->128",
+    "shell256_k1_bf16": "SubMConv3d k1 forward (per-voxel GEMM), 256^3 shell, bf16 128->128",
+    "shell192x4_train_bf16": "SubMConv3d k3 indice build + forward + dinput + dfilter, "
+                             "4 x 192^3 shells, bf16 64->64",
+}
+ELEM = {"f32": 4, "f16": 2, "bf16": 2}
 
 
 def peaks():
@@ -76,12 +94,14 @@ class Clocks:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -115,7 +135,7 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def dist_setup(n_gpus: int):
+def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -143,126 +163,269 @@ def barrier(dist):
         dist.barrier()
 
 
-def algorithmic_bytes(n, K, cin, cout, s, pairs):
-    build = 16 * n + 4 * K * n + 4 * n + 4 * K
-    fwd = s * n * cin + s * n * cout + s * K * cin * cout + 4 * pairs
-    return build, fwd
+class Phase:
+    def __init__(self, name, fn, kind, bytes_alg, flops=0.0, kernels="", launches=1):
+        self.name, self.fn, self.kind = name, fn, kind
+        self.bytes_alg, self.flops, self.kernels = float(bytes_alg), float(flops), kernels
+        self.launches = launches  # kernels of libspc launched by one call of the phase
+        self.graph = None
+        self.ms = []
+
+
+class Case:
+    """Device inputs, preallocated outputs and the timed phases of one workload."""
+
+    def __init__(self, name: str, dev):
+        import sparse_convolution_hash_gb300 as spc
+        from sparse_convolution_hash_gb300 import binding as B
+
+        self.spc, self.B, self.dev = spc, B, dev
+        w = scenes.workload(name)
+        self.w, self.name = w, name
+        self.shape = SHAPES[name.split("_")[0]]
+        c = w["coords"]
+        self.batch = int(c[:, 0].max()) + 1 if c.shape[0] else 1
+        self.n = n = c.shape[0]
+        self.cin, self.cout, self.ks = w["cin"], w["cout"], w["k"]
+        self.K = K = self.ks ** 3
+        self.s = s = ELEM[w["dtype"]]
+        self.dtype = w["dtype"]
+        self.coords_h = torch.from_numpy(c)
+        self.coords = self.coords_h.to(dev)
+        self.x = w["x"].to(dev)
+        self.wt = w["w"].to(dev)
+        self.bias = w["bias"].to(dev) if w["bias"] is not None else None
+        self.status = B.new_status(dev)
+        self.prec = B.SPC_PREC_EXACT
+        self.phases = []
+        self.host_out = []
+        cin, cout = self.cin, self.cout
+
+        if w["subm"]:
+            self.n_out = n
+            if self.ks > 1:
+                self.m = spc.spc_build_indice_map(self.coords, self.batch, self.shape, ksize=self.ks,
+                                                  subm=True, status=self.status)
+                imap, mask = self.m["imap"], self.m["mask"]
+                torch.cuda.synchronize()
+                B.check_status(self.status, "setup build")
+                self.pairs = int(self.m["pair_count"].sum().item())
+                self.phases.append(Phase(
+                    "build", lambda: spc.spc_build_indice_map(
+                        self.coords, self.batch, self.shape, ksize=self.ks, subm=True, out=self.m),
+                    "build", 16 * n + 4 * K * n + 4 * n + 4 * K,
+                    kernels="k_hash_clear, k_hash_insert, k_map_probe", launches=3))
+            else:
+                self.m = None
+                imap = mask = None
+                self.pairs = n
+        else:
+            st, pd = w["stride"], w["pad"]
+            g = B.make_geom(self.ks, st, pd, 1)
+            cap = n * K
+            self.oc_buf = torch.empty((cap, 4), dtype=torch.int32, device=dev)
+            self.n_out_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+            nb = int(B.lib().spc_strided_out_coords_workspace_size(n, ctypes.byref(g)))
+            self.oc_ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+            self.out_shape = (ctypes.c_int32 * 3)()
+            self.geom = g
+
+            def outcoords():
+                code = B.lib().spc_strided_out_coords(
+                    self.coords.data_ptr(), n, self.batch, (ctypes.c_int32 * 3)(*self.shape),
+                    ctypes.byref(self.geom), self.out_shape, self.oc_buf.data_ptr(), cap,
+                    self.n_out_dev.data_ptr(), self.status.data_ptr(), self.oc_ws.data_ptr(),
+                    self.oc_ws.numel(), torch.cuda.current_stream(dev).cuda_stream)
+                assert code == 0, code
+
+            outcoords()
+            torch.cuda.synchronize()
+            B.check_status(self.status, "setup out coords")
+            self.n_out = n_out = int(self.n_out_dev.item())
+            self.oc = self.oc_buf[:n_out]
+            self.m = spc.spc_build_indice_map(self.coords, self.batch, self.shape, ksize=self.ks,
+                                              stride=st, pad=pd, subm=False, out_coords=self.oc,
+                                              with_transpose=True, status=self.status)
+            torch.cuda.synchronize()
+            B.check_status(self.status, "setup strided build")
+            self.pairs = int(self.m["pair_count"].sum().item())
+            imap, mask = self.m["imap"], self.m["mask"]
+            cells = self.batch * int(np.prod(list(self.out_shape)))
+            passes = (max(1, int(np.ceil(np.log2(max(cells, 2))))) + 7) // 8
+            self.phases.append(Phase("outcoords", outcoords, "build", 16 * n + 16 * n_out + 8,
+                                     kernels="k_candidates, k_radix_*, k_unique_*",
+                                     launches=1 + 3 * passes + 3))
+            self.phases.append(Phase(
+                "build", lambda: spc.spc_build_indice_map(
+                    self.coords, self.batch, self.shape, ksize=self.ks, stride=st, pad=pd,
+                    subm=False, out_coords=self.oc, with_transpose=True, out=self.m),
+                "build", 16 * n + 16 * n_out + 4 * K * n_out + 4 * K * n + 4 * n_out + 4 * K,
+                kernels="k_hash_clear, k_hash_insert, k_map_probe<imap_t>", launches=3))
+        n_out, P = self.n_out, self.pairs
+        self.imap, self.mask = imap, mask
+        self.y = torch.empty((n_out, cout), dtype=self.x.dtype, device=dev)
+        nbw = int(B.lib().spc_conv_workspace_size(K, n, n_out, cin, cout, B._DTYPES[self.x.dtype]))
+        self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
+        flops = 2.0 * P * cin * cout
+        bias_b = s * cout if self.bias is not None else 0
+        self.phases.append(Phase(
+            "fwd", lambda: spc.spc_conv_fwd(self.x, self.wt, self.bias, self.imap, self.mask,
+                                            n_out=n_out, precision=self.prec, out=self.y,
+                                            status=self.status, ws=self.conv_ws),
+            "conv", s * n * cin + s * n_out * cout + s * K * cin * cout + 4 * P + bias_b, flops,
+            kernels=self.fwd_kernel(), launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+        self.train = bool(w.get("train"))
+        if self.train:
+            self.dy = w["dy"].to(dev)
+            self.dx = torch.empty((n, cin), dtype=self.x.dtype, device=dev)
+            self.dw = torch.empty((K, cin, cout), dtype=torch.float32, device=dev)
+            nbg = int(B.lib().spc_conv_wgrad_workspace_size(K, n, n_out, cin, cout,
+                                                            B._DTYPES[self.x.dtype]))
+            self.wg_ws = torch.empty(max(nbg, 256), dtype=torch.uint8, device=dev)
+            self.phases.append(Phase(
+                "dgrad", lambda: spc.spc_conv_dgrad(self.dy, self.wt, self.imap,
+                                                    B.SPC_MAP_SUBM_MIRROR, n, mask=self.mask,
+                                                    out=self.dx, status=self.status),
+                "conv", s * n_out * cout + s * n * cin + s * K * cin * cout + 4 * P, flops,
+                kernels=self.fwd_kernel(dgrad=True)))
+            self.phases.append(Phase(
+                "wgrad", lambda: spc.spc_conv_wgrad(self.x, self.dy, self.imap, K, out=self.dw,
+                                                    ws=self.wg_ws),
+                "conv", s * n * cin + s * n_out * cout + 4 * P + 4 * K * cin * cout, flops,
+                kernels="k_wgrad_partial, k_wgrad_reduce", launches=2))
+
+    def fwd_kernel(self, dgrad=False):
+        cred, co = (self.cout, self.cin) if dgrad else (self.cin, self.cout)
+        if self.dtype in ("f16", "bf16") and cred % 64 == 0 and co % 64 == 0 and self.K <= 32:
+            return "k_conv_tc (tcgen05)" + ("" if dgrad else " + k_transpose_w")
+        if cred in (8, 16, 32) and co in (8, 16, 32):
+            return "k_conv_narrow"
+        return "k_gather_gemm_simt"
+
+    def conv_flops(self):
+        return sum(p.flops for p in self.phases)
+
+    def capture(self):
+        for p in self.phases:
+            p.fn()
+        torch.cuda.synchronize()
+        self.B.check_status(self.status, "pre-capture")
+        for p in self.phases:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                p.fn()
+            p.graph = g
+
+    def replay_all(self):
+        for p in self.phases:
+            p.graph.replay()
+
+    # -- end to end through the C ABI from pinned host memory
+    def setup_e2e(self):
+        self.h_in = [(self.coords_h.pin_memory(), self.coords), (self.w["x"].pin_memory(), self.x),
+                     (self.w["w"].pin_memory(), self.wt)]
+        if self.bias is not None:
+            self.h_in.append((self.w["bias"].pin_memory(), self.bias))
+        if self.train:
+            self.h_in.append((self.w["dy"].pin_memory(), self.dy))
+        outs = [self.y] + ([self.dx, self.dw] if self.train else [])
+        self.h_out = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in outs]
+        self.h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
+        self.d2h = sum(h.numel() * h.element_size() for h, _ in self.h_out)
+
+    def e2e_step(self):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        for p in self.phases:
+            p.fn()
+        for h, d in self.h_out:
+            h.copy_(d, non_blocking=True)
+
+
+def roofline(p: Phase, ms: float, hbm: float, tc_peak: float, alu_peak: float, dtype: str,
+             prec_tf32: bool):
+    t_hbm = p.bytes_alg / (hbm * 1e9)
+    if p.kind != "conv":
+        bound, peak, ach, unit = "hbm", hbm, p.bytes_alg / (ms * 1e-3) / 1e9, "GB/s"
+        t_bound = t_hbm
+    else:
+        if dtype == "f32" and not prec_tf32:
+            cpeak, cbound = alu_peak, "alu"
+        else:
+            cpeak, cbound = (tc_peak * (1.1 / 2.25) if dtype == "f32" else tc_peak), "tensor"
+        t_c = p.flops / (cpeak * 1e12)
+        if t_c >= t_hbm:
+            bound, peak, ach, unit, t_bound = cbound, cpeak, p.flops / (ms * 1e-3) / 1e12, "TFLOP/s", t_c
+        else:
+            bound, peak, ach, unit, t_bound = "hbm", hbm, p.bytes_alg / (ms * 1e-3) / 1e9, "GB/s", t_hbm
+    return {"bound": bound, "achieved": round(ach, 3), "peak": round(peak, 1), "unit": unit,
+            "frac": round(ach / peak, 4), "roofline_ms": round(t_bound * 1e3, 5)}
 
 
 def run_ours(args, rank, world, local, dist):
-    import sparse_convolution_hash_gb300 as spc
-    from sparse_convolution_hash_gb300 import binding
-
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = scenes.workload(WORKLOAD)
-    coords_h = torch.from_numpy(w["coords"])
-    n = coords_h.shape[0]
-    cin, cout, K = w["cin"], w["cout"], 27
-    coords = coords_h.to(dev)
-    x = w["x"].to(dev)
-    wt = w["w"].to(dev)
-    ws = torch.empty(max(binding.spc_indice_map_workspace_size(n), 256), dtype=torch.uint8,
-                     device=dev)
-    status = binding.new_status(dev)
+    case = Case(args.workload, dev)
+    case.capture()
+    for _ in range(args.warmup):
+        case.replay_all()
+    torch.cuda.synchronize()
+    case.B.check_status(case.status, "bench warmup")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    m = spc.spc_build_indice_map(coords, BATCH, SHAPE, ksize=3, subm=True, status=status, ws=ws)
-    y = spc.spc_conv_fwd(x, wt, None, m["imap"], m["mask"])
-    torch.cuda.synchronize()
-    binding.check_status(status, "bench build")
-    pairs = int(m["pair_count"].sum().item())
-
-    def build():
-        spc.spc_build_indice_map(coords, BATCH, SHAPE, ksize=3, subm=True, out=m)
-
-    def fwd():
-        spc.spc_conv_fwd(x, wt, None, m["imap"], m["mask"], out=y)
-
-    # The step's launches are captured once as CUDA graphs (the C ABI allocates
-    # nothing and only enqueues on the current stream), so the timed replays
-    # measure GPU work, not the host's Python and ctypes overhead.
-    g_build, g_fwd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_build):
-        build()
-    with torch.cuda.graph(g_fwd):
-        fwd()
-    for _ in range(args.warmup):
-        g_build.replay()
-        g_fwd.replay()
-    torch.cuda.synchronize()
-    binding.check_status(status, "bench warmup")
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    nph = len(case.phases)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     barrier(dist)
     torch.cuda.synchronize()
     with Clocks(local) as clk:
         # keep the device busy while the host enqueues all steps, so that no
         # host gap falls inside a timed step
-        torch.cuda._sleep(int(4e6) * args.steps // 10 + int(2e6))
+        torch.cuda._sleep(int(3e5) * args.steps * nph + int(2e6))
         for i in range(args.steps):
             flush.zero_()
-            ev[i][0].record(stream)
-            g_build.replay()
-            ev[i][1].record(stream)
-            g_fwd.replay()
-            ev[i][2].record(stream)
+            for j, p in enumerate(case.phases):
+                ev[i][j].record(stream)
+                p.graph.replay()
+            ev[i][nph].record(stream)
         torch.cuda.synchronize()
     barrier(dist)
-    binding.check_status(status, "bench timed")
-    build_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    total_ms = sum(b + f for b, f in zip(build_ms, fwd_ms))
-    total_ms = reduce_max(total_ms, dist, dev)
+    case.B.check_status(case.status, "bench timed")
+    for j, p in enumerate(case.phases):
+        p.ms = [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
+    total_ms = reduce_max(sum(sum(p.ms) for p in case.phases), dist, dev)
     ms_step = total_ms / args.steps
-    flops = 2.0 * pairs * cin * cout
+    flops = case.conv_flops()
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
-    # end to end through the C ABI from pinned host buffers
-    coords_p = coords_h.pin_memory()
-    x_p = w["x"].pin_memory()
-    w_p = w["w"].pin_memory()
-    y_p = torch.empty((n, cout), dtype=x.dtype).pin_memory()
-    e2e_steps = max(1, min(args.steps, 20))
-    c_d, x_d, w_d = torch.empty_like(coords), torch.empty_like(x), torch.empty_like(wt)
-    y_d = torch.empty_like(y)
-
-    def e2e_step():
-        # the calls a user makes: copy in, build the map, convolve, copy out
-        c_d.copy_(coords_p, non_blocking=True)
-        x_d.copy_(x_p, non_blocking=True)
-        w_d.copy_(w_p, non_blocking=True)
-        spc.spc_build_indice_map(c_d, BATCH, SHAPE, ksize=3, subm=True, out=m)
-        spc.spc_conv_fwd(x_d, w_d, None, m["imap"], m["mask"], out=y_d)
-        y_p.copy_(y_d, non_blocking=True)
-
+    case.setup_e2e()
     for _ in range(2):
-        e2e_step()
+        case.e2e_step()
     torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 20))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        case.e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
+    case.B.check_status(case.status, "bench e2e")
     e2e_ms = reduce_max(e0.elapsed_time(e1), dist, dev) / e2e_steps
-    h2d = coords_h.numel() * 4 + w["x"].numel() * w["x"].element_size() + w["w"].numel() * w["w"].element_size()
-    d2h = n * cout * x.element_size()
 
     hbm, bf16_tf, peak_src = peaks()
-    s = x.element_size()
-    b_build, b_fwd = algorithmic_bytes(n, K, cin, cout, s, pairs)
-    build_avg = sum(build_ms) / len(build_ms)
-    fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    if build_avg >= fwd_avg:
-        dom, dom_bytes, dom_ms = "spc_build_indice_map (hash clear + insert + probe)", b_build, build_avg
-    else:
-        dom, dom_bytes, dom_ms = "spc_conv_fwd", b_fwd, fwd_avg
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    props = torch.cuda.get_device_properties(dev)
+    alu_peak = props.multi_processor_count * 128 * 2 * 2.07e9 / 1e12  # FP32 FMA lanes x 2 x max clock
+    phases = {}
+    for p in case.phases:
+        avg = sum(p.ms) / len(p.ms)
+        r = roofline(p, avg, hbm, bf16_tf, alu_peak, case.dtype, case.prec == case.B.SPC_PREC_TF32)
+        phases[p.name] = {"ms": round(avg, 5), "kernels": p.kernels, **r}
+        if p.kind == "conv":
+            phases[p.name]["tflops"] = round(p.flops / (avg * 1e-3) / 1e12, 3)
+    dom = max(case.phases, key=lambda p: sum(p.ms))
+    dom_r = phases[dom.name]
     clocks = clk.summary()
-
+    build_ms = sum(phases[k]["ms"] for k in ("outcoords", "build") if k in phases)
     line = {
         "metric": METRIC,
         "value": round(value, 4),
@@ -274,97 +437,112 @@ def run_ours(args, rank, world, local, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
-        "data": "synthetic (seeded LiDAR-like scene, random-init weights)",
+        "dtype": case.dtype,
+        "data": "synthetic (seeded scene, random-init weights)",
         "config": {
-            "workload": "lidar_subm_f16: SubMConv3d k3 indice build + forward, batch 2, "
-                        "41x1600x1408 grid, 120000 voxels, fp16 16->16, no bias",
-            "n_voxels": n, "pairs": pairs, "cin": cin, "cout": cout, "K": K,
+            "workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+            "n_voxels": case.n, "n_out": case.n_out, "pairs": case.pairs, "cin": case.cin,
+            "cout": case.cout, "K": case.K,
             "l2": "flushed between timed steps (256 MiB write, outside the events)",
+            "timing": "CUDA-graph replay per phase, CUDA events on the launching stream",
             "parallelism": f"replicas x{world}",
         },
-        "indice_map_mvoxel_s": round(world * n / (build_avg * 1e-3) / 1e6, 2),
-        "conv_fwd_tflops": round(world * flops / (fwd_avg * 1e-3) / 1e12, 4),
-        "build_ms": round(build_avg, 5),
-        "fwd_ms": round(fwd_avg, 5),
-        "roofline": {
-            "kernel": dom,
-            "bound": "hbm",
-            "achieved": round(achieved, 1),
-            "peak": hbm,
-            "unit": "GB/s",
-            "frac": round(achieved / hbm, 4),
-            "traffic": None,
-            "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-            "alg_bytes_per_launch": dom_bytes,
-        },
+        "indice_map_mvoxel_s": round(world * case.n / (build_ms * 1e-3) / 1e6, 2) if build_ms else None,
+        "phases": phases,
+        "roofline": {"kernel": f"{dom.name}: {dom.kernels}", "bound": dom_r["bound"],
+                     "achieved": dom_r["achieved"], "peak": dom_r["peak"], "unit": dom_r["unit"],
+                     "frac": dom_r["frac"], "traffic": None,
+                     "peak_source": f"{peak_src} ({'hbm_gbs burst copy' if dom_r['unit'] == 'GB/s' else 'bf16_tflops burst' if dom_r['bound'] == 'tensor' else 'FP32 lanes x clock'})",
+                     "alg_bytes_per_launch": dom.bytes_alg, "alg_flops_per_launch": dom.flops},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(case.h2d),
+                "d2h_bytes_per_step": int(case.d2h)},
+        "gpu_launches": args.steps * sum(p.launches for p in case.phases),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, pairs, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(case, budget_s=args.cpu_seconds)
     return line
 
 
-def cpu_baseline(w, pairs, budget_s=10.0):
-    """The oracle as it stands, timed on the host: whole-workload steps until the budget."""
+def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, pad=0):
+    """Times the oracle on a bounded sample; returns (TFLOP/s, description)."""
     import oracle
 
     oracle.build()
-    coords = w["coords"]
-    x64, w64 = oracle.f64(w["x"]), oracle.f64(w["w"])
-    flops = 2.0 * pairs * w["cin"] * w["cout"]
-    reps, t0 = 0, time.perf_counter()
+    c = case_w["coords"]
+    n = c.shape[0]
+    x64, w64 = oracle.f64(case_w["x"]), oracle.f64(case_w["w"])
+    b64 = oracle.f64(case_w["bias"]) if case_w["bias"] is not None else None
+    cin, cout = case_w["cin"], case_w["cout"]
+    t0 = time.perf_counter()
+    if subm:
+        imap, cnt = oracle.subm_map(c, batch, shape, ks)
+    else:
+        oc = oracle.strided_out_coords(c, batch, shape, ks, stride, pad, 1)
+        imap, _, cnt = oracle.strided_map(c, oc, batch, shape, ks, stride, pad, 1, False)
+    t_map = time.perf_counter() - t0
+    n_out = imap.shape[1]
+    per_row = 2.0 * float(cnt.sum()) / max(n_out, 1) * cin * cout  # flops per output row
+    # rows so that the forward sample takes about the budget at ~1 GFLOP/s
+    rows = int(min(n_out, max(64, budget_s * 1.0e9 / max(per_row, 1.0))))
+    sel = np.linspace(0, n_out - 1, rows).astype(np.int64) if rows < n_out else None
+    reps, flops, t_fwd = 0, 0.0, 0.0
+    t1 = time.perf_counter()
     while True:
-        imap, _ = oracle.subm_map(coords, BATCH, SHAPE, 3)
-        oracle.conv_fwd(x64, w64, None, imap)
+        if sel is None:
+            oracle.conv_fwd(x64, w64, b64, imap)
+            flops += 2.0 * float(cnt.sum()) * cin * cout
+        else:
+            oracle.conv_fwd(x64, w64, b64, imap, rows=sel)
+            flops += 2.0 * float((imap[:, sel] >= 0).sum()) * cin * cout
         reps += 1
-        if time.perf_counter() - t0 >= budget_s:
+        t_fwd = time.perf_counter() - t1
+        if t_fwd >= budget_s or sel is not None:
             break
-    dt = time.perf_counter() - t0
-    return {"value": round(reps * flops / dt / 1e12, 8), "unit": "TFLOP/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{reps} whole steps (indice map + fp64 forward over all {coords.shape[0]} "
-                      f"voxels) in {dt:.1f} s, single thread",
-            "ms_per_step": round(1e3 * dt / reps, 2)}
+    frac = (len(sel) if sel is not None else n_out) / max(n_out, 1)
+    t = t_map * frac * (reps if sel is None else 1) + t_fwd
+    what = (f"{reps} whole steps (map + fp64 forward of all {n_out} rows)" if sel is None else
+            f"map over all {n} voxels ({t_map:.2f} s, charged pro rata) + fp64 forward of "
+            f"{len(sel)} of {n_out} rows")
+    return flops / t / 1e12, f"{what}, {t:.1f} s, single thread"
+
+
+def cpu_baseline(case, budget_s=10.0):
+    w = case.w
+    val, what = cpu_sample(w, case.batch, case.shape, case.ks, w["subm"], case.pairs, budget_s,
+                           w.get("stride", 1), w.get("pad", 0))
+    return {"value": round(val, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": what}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    w = scenes.workload(WORKLOAD)
-    import oracle
-
-    oracle.build()
-    coords = w["coords"]
-    x64, w64 = oracle.f64(w["x"]), oracle.f64(w["w"])
-    imap, cnt = oracle.subm_map(coords, BATCH, SHAPE, 3)
-    pairs = int(cnt.sum())
-    flops = 2.0 * pairs * w["cin"] * w["cout"]
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm state; warm-up steps would only repeat the work
-    times = []
+    w = scenes.workload(args.workload)
+    kind = args.workload.split("_")[0]
+    shape = SHAPES[kind]
+    c = w["coords"]
+    batch = int(c[:, 0].max()) + 1
+    vals = []
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        t0 = time.perf_counter()
-        imap, _ = oracle.subm_map(coords, BATCH, SHAPE, 3)
-        oracle.conv_fwd(x64, w64, None, imap)
-        times.append(time.perf_counter() - t0)
-    tot = sum(times)
-    value = args.steps * flops / tot / 1e12
+        v, what = cpu_sample(w, batch, shape, w["k"], w["subm"], None,
+                             args.cpu_seconds / max(args.steps, 1), w.get("stride", 1),
+                             w.get("pad", 0))
+        vals.append(v)
+    tot = time.perf_counter() - t0
+    value = statistics.mean(vals)
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded LiDAR-like scene, random-init weights)",
-        "config": {"workload": "lidar_subm_f16: SubMConv3d k3 indice build + forward, batch 2, "
-                               "41x1600x1408 grid, 120000 voxels, fp16 16->16, no bias",
-                   "n_voxels": int(coords.shape[0]), "pairs": pairs},
+        "data": "synthetic (seeded scene, random-init weights)",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "n_voxels": int(c.shape[0])},
         "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} whole steps, single thread"},
+                         "sample": f"per step: {what}"},
         "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -376,12 +554,12 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    rank, world, local, dist = dist_setup(args.gpus)
+    args.warmup = max(args.warmup, 3)
+    rank, world, local, dist = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

@@ -269,7 +269,8 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
         a.cred = cin;
         a.n_total = cout;
         a.mirror = 0;
-        return conv_gather_tc(a, dt, st);
+        s = conv_gather_tc(a, dt, st);
+        if (s != SPC_ERR_UNSUPPORTED) return s;
     }
     return run_gather(p, dt, st);
 }
@@ -319,7 +320,8 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
         a.cred = cout;
         a.n_total = cin;
         a.mirror = p.mirror;
-        return conv_gather_tc(a, dt, st);
+        const spc_status s2 = conv_gather_tc(a, dt, st);
+        if (s2 != SPC_ERR_UNSUPPORTED) return s2;
     }
     return run_gather(p, dt, st);
 }

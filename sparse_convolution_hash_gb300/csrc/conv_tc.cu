@@ -1,18 +1,23 @@
 // conv_tc.cu -- gathered implicit GEMM on the 5th-generation tensor cores
 // (tcgen05, accumulators in tensor memory) for wide channels.
 //
-// Output-stationary: a CTA owns 128 output rows (the MMA's M) x BN output
-// channels.  It first ORs its rows' offset masks, so offsets that no row of
+// Output-stationary: a CTA owns 256 output rows (two 128-row MMA tiles with
+// their own accumulators, sharing every weight stage) x BN output channels.  It first ORs its rows' offset masks, so offsets that no row of
 // the tile uses are skipped, and reads its rows' map entries for the remaining
 // offsets.  The K loop then runs over (active offset, 128-byte channel chunk):
-//   producers (warps 0-3, one row each) gather the 128 input rows of that
-//     offset with 16-byte cp.async copies straight into a 128-byte-swizzled
-//     K-major shared-memory stage (rows with no neighbour are zero-filled by
-//     the copy itself), plus the matching BN x 128-byte weight tile;
-//   one thread of warp 4 waits for the stage, issues four tcgen05.mma (K = 32
-//     bytes each) into the fp32 accumulator in tensor memory, and commits the
-//     stage back to the producers.
-// All offsets accumulate in tensor memory; the epilogue (warps 0-3) reads each
+//   warps 0-7 gather the 256 input rows of that offset with 16-byte cp.async
+//     copies straight into a 128-byte-swizzled K-major shared-memory stage (a
+//     warp instruction copies four whole 128-byte row segments; rows with no
+//     neighbour are zero-filled by the copy itself); each thread's copies
+//     arrive on the stage's mbarrier when they land, so no thread waits for
+//     its own data;
+//   one thread of warp 8 loads the BN x 128-byte weight tile with a 2-D TMA
+//     load that completes on the same barrier;
+//   one thread of warp 9 waits for the stage, fences the copies into the
+//     async proxy, issues 2 x 4 tcgen05.mma (one per 128-row half, K = 32
+//     bytes each) into the fp32 accumulators in tensor memory, and commits
+//     the stage back to the producers.
+// All offsets accumulate in tensor memory; the epilogue (warps 0-7) reads each
 // row's accumulators with tcgen05.ld, adds the bias, rounds once and stores the
 // row.  Every output row is written once: no atomics, run-to-run identical.
 //
@@ -22,8 +27,11 @@
 // [N][K] K-major for that product).
 //
 // Every barrier wait is bounded (2 s of wall time); a wait that runs out sets
-// SPC_ERR_TIMEOUT in the status word, the CTA drains its copies, waits for its
-// MMAs, frees its tensor memory and returns.
+// SPC_ERR_TIMEOUT in the status word, the CTA waits (bounded) for the copies it
+// issued and for its MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -31,8 +39,10 @@ namespace spc {
 
 namespace {
 
-constexpr int kRowsPerCta = 128;
-constexpr int kThreads = 160;
+constexpr int kHalf = 128;                 // rows per MMA (M)
+constexpr int kRowsPerCta = 2 * kHalf;     // two accumulators share each weight stage
+constexpr int kEpilogue = 256;             // warps 0-7: prologue and epilogue, one row each
+constexpr int kThreads = kEpilogue + 64;   // warp 8: weight TMA; warp 9: TMEM owner, MMA issuer
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <typename T, int BN, int STAGES>
@@ -42,6 +52,7 @@ struct TcShape {
     static constexpr int A_BYTES = kRowsPerCta * 128;
     static constexpr int B_BYTES = BN * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
     static size_t smem_bytes(int K)
     {
         return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
@@ -55,7 +66,8 @@ template <> struct TcKind<__nv_bfloat16> { static constexpr int kind = 0; static
 template <> struct TcKind<float> { static constexpr int kind = 1; static constexpr uint32_t fmt = 2; };
 
 template <typename T, int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1) k_conv_tc(TcArgs a)
+__global__ void __launch_bounds__(kThreads, 1)
+k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 {
     using S = TcShape<T, BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -75,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_tc(TcArgs a)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], kRowsPerCta);
+            ptx::mbar_init(&full[s], kEpilogue + 1);  // 256 copy completions + the weight TMA
             ptx::mbar_init(&empty[s], 1);
         }
         ptx::mbar_init(done, 1);
@@ -84,15 +96,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_tc(TcArgs a)
         s_ctrl[2] = 0;
         ptx::mbar_init_fence();
     }
-    if (warp == 4) {
-        ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[3]), BN);
+    if (warp == 8 && lane == 0) ptx::prefetch_tmap(&tma_b);
+    if (warp == 9) {
+        ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[3]), S::TMEM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
 
-    // union of the tile's row masks
+    // union of the tile's row masks (thread t owns row t of the tile)
     const int64_t row = row0 + tid;
     const bool rvalid = tid < kRowsPerCta && row < a.rows;
     uint32_t m = 0;
@@ -117,93 +130,122 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_tc(TcArgs a)
     }
     __syncthreads();
     const int nact = s_ctrl[0];
+    if (tid < kRowsPerCta) {
+        // this row's map entries for the tile's active offsets (all loads in
+        // flight before the first store); misses become the out-of-range row
+        // in_rows, which the gather fills with zeros
+        int32_t iv[32];
+#pragma unroll
+        for (int ai = 0; ai < 32; ++ai) {
+            iv[ai] = -1;
+            if (ai < nact) {
+                const int k = s_active[ai];
+                if (rvalid && ((m >> k) & 1u)) {
+                    const int mk = a.mirror ? K - 1 - k : k;
+                    iv[ai] = a.map ? __ldg(a.map + (int64_t)mk * a.rows + row) : (int32_t)row;
+                }
+            }
+        }
+#pragma unroll
+        for (int ai = 0; ai < 32; ++ai)
+            if (ai < nact) s_idx[ai * kRowsPerCta + tid] = iv[ai] < a.in_rows ? iv[ai] : -1;
+    }
+    __syncthreads();
     const int kchunks = a.cred / S::CH;
     const int n_iter = nact * kchunks;
     const uint32_t tmem = (uint32_t)s_ctrl[3];
-    const uint8_t* in = static_cast<const uint8_t*>(a.in);
-    const uint8_t* bmat = static_cast<const uint8_t*>(a.b);
 
-    if (tid < kRowsPerCta) {
-        // ---------------------------------------------------------- producers
-        for (int ai = 0; ai < nact; ++ai) {
-            const int k = s_active[ai];
-            int32_t i = -1;
-            if (rvalid && ((m >> k) & 1u)) {
-                const int mk = a.mirror ? K - 1 - k : k;
-                i = a.map ? a.map[(int64_t)mk * a.rows + row] : (int32_t)row;
-                if (i >= a.in_rows) i = -1;
-            }
-            s_idx[ai * kRowsPerCta + tid] = i;
-        }
-        bool ok = true;
+    const uint8_t* in = static_cast<const uint8_t*>(a.in);
+    if (tid < kEpilogue) {
+        // -------------------------------------------------- row-gather producers
+        // A stage: 256 rows x 8 chunks of 16 bytes; chunk e = j * 256 + tid, so a
+        // warp instruction copies four whole 128-byte row segments.  Each
+        // thread's copies arrive on the stage's barrier when they complete, so
+        // the thread never waits for its own data, only for a free stage.
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % STAGES;
-            if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitNs)) {
-                ok = false;
+            bool ok = true;
+            if (it >= STAGES) ok = ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitNs);
+            if (!ok) {
+                atomicExch(&s_ctrl[1], 1);
                 break;
             }
             const int ai = it / kchunks;
             const int c0 = (it % kchunks) * S::CH;
-            const int k = s_active[ai];
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
-            const uint32_t b_base = a_base + S::A_BYTES;
-            const int32_t i = s_idx[ai * kRowsPerCta + tid];
-            const uint8_t* src = i >= 0 ? in + ((int64_t)i * a.cred + c0) * S::ELEM : in;
-            const uint32_t nbytes = i >= 0 ? 16u : 0u;
-            const uint32_t arow = a_base + (uint32_t)tid * 128u;
+            const int32_t* idx = s_idx + ai * kRowsPerCta;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                ptx::cp_async16(arow + ((uint32_t)(ch ^ (tid & 7)) << 4), src + (i >= 0 ? ch * 16 : 0),
-                                nbytes);
-            const uint8_t* bk = bmat + (((int64_t)k * a.n_total + n0) * a.cred + c0) * S::ELEM;
-#pragma unroll
-            for (int e = tid; e < BN * 8; e += kRowsPerCta) {
+            for (int j = 0; j < kRowsPerCta * 8 / kEpilogue; ++j) {
+                const int e = j * kEpilogue + tid;
                 const int r = e >> 3, ch = e & 7;
-                ptx::cp_async16(b_base + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4),
-                                bk + (int64_t)r * a.cred * S::ELEM + ch * 16, 16u);
+                const int32_t i = idx[r];
+                const uint8_t* src = i >= 0 ? in + ((int64_t)i * a.cred + c0) * S::ELEM + ch * 16 : in;
+                ptx::cp_async16(a_base + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4), src,
+                                i >= 0 ? 16u : 0u);
             }
-            ptx::cp_async_commit();
-            if (it >= STAGES - 1) {
-                ptx::cp_async_wait<STAGES - 1>();
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(&full[(it - (STAGES - 1)) % STAGES]);
+            ptx::cp_async_arrive_noinc(&full[s]);
+        }
+        ptx::cp_async_wait_all();  // nothing of ours may still land when the CTA ends
+    } else if (warp == 8) {
+        // -------------------------------------------------- weight producer (TMA)
+        int issued = 0;
+        if (lane == 0) {
+            for (int it = 0; it < n_iter; ++it) {
+                const int s = it % STAGES;
+                if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitNs)) {
+                    atomicExch(&s_ctrl[1], 1);
+                    break;
+                }
+                const int ai = it / kchunks;
+                const int c0 = (it % kchunks) * S::CH;
+                const int k = s_active[ai];
+                const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
+                ptx::mbar_arrive_expect_tx(&full[s], S::B_BYTES);
+                ptx::tma_tile2d(a_base + S::A_BYTES, &tma_b, c0, k * a.n_total + n0, &full[s]);
+                ++issued;
             }
+            // make sure no copy issued above is still landing before the CTA ends
+            const int first = issued > STAGES ? issued - STAGES : 0;
+            for (int it = first; it < issued; ++it)
+                ptx::mbar_wait(&full[it % STAGES], (it / STAGES) & 1, kWaitNs);
         }
-        ptx::cp_async_wait_all();
-        ptx::fence_proxy_async_smem();
-        if (ok) {
-            for (int j = n_iter - (STAGES - 1) > 0 ? n_iter - (STAGES - 1) : 0; j < n_iter; ++j)
-                ptx::mbar_arrive(&full[j % STAGES]);
-        } else {
-            atomicExch(&s_ctrl[1], 1);
-        }
-    } else if (warp == 4 && lane == 0) {
+    } else if (warp == 9 && lane == 0) {
         // ------------------------------------------------------- MMA issuer
-        const uint32_t idesc = ptx::idesc_make(TcKind<T>::fmt, kRowsPerCta, BN);
+        const uint32_t idesc = ptx::idesc_make(TcKind<T>::fmt, kHalf, BN);
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % STAGES;
             if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, kWaitNs)) {
                 atomicExch(&s_ctrl[1], 1);
                 break;
             }
+            // the rows arrived through generic-proxy copies: order them before
+            // the tensor core's async-proxy reads
+            ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
-            const uint64_t ad = ptx::desc_k_sw128(a_base);
+            const uint64_t a0 = ptx::desc_k_sw128(a_base);
+            const uint64_t a1 = ptx::desc_k_sw128(a_base + kHalf * 128);
             const uint64_t bd = ptx::desc_k_sw128(a_base + S::A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // 32 bytes of K per instruction
-                ptx::mma<TcKind<T>::kind>(tmem, ad + 2 * kk, bd + 2 * kk, idesc,
-                                          (it | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per instruction
+                const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
+                ptx::mma<TcKind<T>::kind>(tmem, a0 + 2 * kk, bd + 2 * kk, idesc, acc);
+                ptx::mma<TcKind<T>::kind>(tmem + BN, a1 + 2 * kk, bd + 2 * kk, idesc, acc);
+            }
             ptx::mma_commit(&empty[s]);
         }
         ptx::mma_commit(done);  // completes once every MMA issued above has finished
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (tid < kRowsPerCta) {
+    if (tid < kEpilogue) {
         const bool waited = ptx::mbar_wait(done, 0, kWaitNs);
         ptx::tc_fence_after();
         const bool aborted = __any_sync(FULL_MASK, !waited || s_ctrl[1] != 0);
+        // warp w reads TMEM lanes 32*(w%4).. of accumulator w/4 (rows 128*(w/4) + ...)
+        const int half = warp >> 2, quarter = warp & 3;
+        const int64_t erow = row0 + half * kHalf + quarter * 32 + lane;
+        const bool evalid = erow < a.rows;
         if (aborted) {
             if (tid == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         } else {
@@ -213,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_tc(TcArgs a)
             for (int c = 0; c < BN; c += 32) {
                 uint32_t v[32];
                 if (n_iter > 0) {
-                    ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+                    ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * BN + c), v);
                     ptx::tmem_ld_wait();
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0u;
                 }
-                if (rvalid) {
-                    T* dst = out + row * a.n_total + n0 + c;
+                if (evalid) {
+                    T* dst = out + erow * a.n_total + n0 + c;
                     alignas(16) T o[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -238,9 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_tc(TcArgs a)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 9) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, BN);
+        ptx::tmem_dealloc(tmem, S::TMEM_COLS);
     }
 }
 
@@ -264,10 +306,50 @@ __global__ void __launch_bounds__(256) k_transpose_w(const T* __restrict__ w, T*
     }
 }
 
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
+EncodeFn encoder()
+{
+    static EncodeFn fn = []() -> EncodeFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeFn>(p);
+    }();
+    return fn;
+}
+
+template <typename T> struct TmaType;
+template <> struct TmaType<__half> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; };
+template <> struct TmaType<__nv_bfloat16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; };
+template <> struct TmaType<float> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; };
+
+// 2-D row-major [rows, cols] tensor, boxes of 128 bytes x box_rows, 128-byte swizzle.
+template <typename T>
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows)
+{
+    EncodeFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * sizeof(T)};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(T)), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, TmaType<T>::v, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T, int BN, int STAGES>
 spc_status launch_tc(const TcArgs& a, cudaStream_t st)
 {
     using S = TcShape<T, BN, STAGES>;
+    CUtensorMap tb;
+    if (!make_tmap<T>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN))
+        return SPC_ERR_UNSUPPORTED;
     const size_t smem = S::smem_bytes(a.K);
     auto kern = k_conv_tc<T, BN, STAGES>;
     static bool configured[64] = {};
@@ -280,7 +362,7 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
         configured[dev] = true;
     }
     dim3 grid((unsigned)ceil_div(a.rows, kRowsPerCta), (unsigned)(a.n_total / BN));
-    kern<<<grid, kThreads, smem, st>>>(a);
+    kern<<<grid, kThreads, smem, st>>>(a, tb);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }
@@ -288,8 +370,8 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
 template <typename T>
 spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
 {
-    // stage counts keep two CTAs' shared memory on one SM
-    if (a.n_total % 128 == 0) return launch_tc<T, 128, 3>(a, st);
+    // one CTA per SM; stage counts fill its shared memory
+    if (a.n_total % 128 == 0) return launch_tc<T, 128, 4>(a, st);
     return launch_tc<T, 64, 4>(a, st);
 }
 

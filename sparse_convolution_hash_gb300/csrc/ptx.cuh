@@ -63,12 +63,58 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+// Four rows (row coordinates r0..r3, each one box row high) of a 2-D tensor
+// starting at column x, written to consecutive 128-byte rows at dst with the
+// tensor map's swizzle; out-of-range rows are filled with zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// One box of a 2-D tensor at (x, y).
+__device__ __forceinline__ void tma_tile2d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                           uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                  "r"(src_bytes)
+                 : "memory");
+}
+
+// The mbarrier receives one arrival when every cp.async issued so far by this
+// thread has completed (its expected count must include that arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
 
