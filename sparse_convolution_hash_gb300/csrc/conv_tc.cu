@@ -5,19 +5,19 @@
 // their own accumulators, sharing every weight stage) x BN output channels.  It first ORs its rows' offset masks, so offsets that no row of
 // the tile uses are skipped, and reads its rows' map entries for the remaining
 // offsets.  The K loop then runs over (active offset, 128-byte channel chunk):
-//   warps 0-7 gather the 256 input rows of that offset with 16-byte cp.async
+//   warps 0-15 gather the 256 input rows of that offset with 16-byte cp.async
 //     copies straight into a 128-byte-swizzled K-major shared-memory stage (a
 //     warp instruction copies four whole 128-byte row segments; rows with no
 //     neighbour are zero-filled by the copy itself); each thread's copies
 //     arrive on the stage's mbarrier when they land, so no thread waits for
 //     its own data;
-//   one thread of warp 8 loads the BN x 128-byte weight tile with a 2-D TMA
+//   one thread of warp 16 loads the BN x 128-byte weight tile with a 2-D TMA
 //     load that completes on the same barrier;
-//   one thread of warp 9 waits for the stage, fences the copies into the
+//   one thread of warp 17 waits for the stage, fences the copies into the
 //     async proxy, issues 2 x 4 tcgen05.mma (one per 128-row half, K = 32
 //     bytes each) into the fp32 accumulators in tensor memory, and commits
 //     the stage back to the producers.
-// All offsets accumulate in tensor memory; the epilogue (warps 0-7) reads each
+// All offsets accumulate in tensor memory; the epilogue (warps 0-15) reads each
 // row's accumulators with tcgen05.ld, adds the bias, rounds once and stores the
 // row.  Every output row is written once: no atomics, run-to-run identical.
 //
@@ -41,8 +41,9 @@ namespace {
 
 constexpr int kHalf = 128;                 // rows per MMA (M)
 constexpr int kRowsPerCta = 2 * kHalf;     // two accumulators share each weight stage
-constexpr int kEpilogue = 256;             // warps 0-7: prologue and epilogue, one row each
-constexpr int kThreads = kEpilogue + 64;   // warp 8: weight TMA; warp 9: TMEM owner, MMA issuer
+constexpr int kWorkers = 512;              // warps 0-15: row gathers, then the epilogue
+constexpr int kThreads = kWorkers + 64;    // warp 16: weight TMA; warp 17: TMEM owner, MMA issuer
+constexpr int kTmaWarp = kWorkers / 32, kMmaWarp = kTmaWarp + 1;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <typename T, int BN, int STAGES>
@@ -87,7 +88,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], kEpilogue + 1);  // 256 copy completions + the weight TMA
+            ptx::mbar_init(&full[s], kWorkers + 1);  // 512 copy completions + the weight TMA
             ptx::mbar_init(&empty[s], 1);
         }
         ptx::mbar_init(done, 1);
@@ -96,8 +97,8 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
         s_ctrl[2] = 0;
         ptx::mbar_init_fence();
     }
-    if (warp == 8 && lane == 0) ptx::prefetch_tmap(&tma_b);
-    if (warp == 9) {
+    if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tma_b);
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[3]), S::TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -111,7 +112,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
     uint32_t m = 0;
     if (tid < kRowsPerCta) {
         if (rvalid) {
-            m = a.mask ? a.mask[row] : kmask;
+            m = a.mask ? __ldcs(a.mask + row) : kmask;  // read once: evict first
             if (a.mask && a.mirror) m = __brev(m) >> (32 - K);
             m &= kmask;
         }
@@ -142,7 +143,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
                 const int k = s_active[ai];
                 if (rvalid && ((m >> k) & 1u)) {
                     const int mk = a.mirror ? K - 1 - k : k;
-                    iv[ai] = a.map ? __ldg(a.map + (int64_t)mk * a.rows + row) : (int32_t)row;
+                    iv[ai] = a.map ? __ldcs(a.map + (int64_t)mk * a.rows + row) : (int32_t)row;
                 }
             }
         }
@@ -156,12 +157,15 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
     const uint32_t tmem = (uint32_t)s_ctrl[3];
 
     const uint8_t* in = static_cast<const uint8_t*>(a.in);
-    if (tid < kEpilogue) {
+    if (tid < kWorkers) {
         // -------------------------------------------------- row-gather producers
-        // A stage: 256 rows x 8 chunks of 16 bytes; chunk e = j * 256 + tid, so a
-        // warp instruction copies four whole 128-byte row segments.  Each
+        // A stage: 256 rows x 8 chunks of 16 bytes; chunk e = j * 512 + tid, so a
+        // warp instruction copies four whole 128-byte row segments.  Sixteen
+        // warps keep enough copies in flight to cover L2 latency.  Each
         // thread's copies arrive on the stage's barrier when they complete, so
         // the thread never waits for its own data, only for a free stage.
+        // feature rows are re-read by up to K output rows: keep them in L2
+        const uint64_t keep = ptx::policy_evict_last();
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % STAGES;
             bool ok = true;
@@ -175,18 +179,18 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
             const int32_t* idx = s_idx + ai * kRowsPerCta;
 #pragma unroll
-            for (int j = 0; j < kRowsPerCta * 8 / kEpilogue; ++j) {
-                const int e = j * kEpilogue + tid;
+            for (int j = 0; j < kRowsPerCta * 8 / kWorkers; ++j) {
+                const int e = j * kWorkers + tid;
                 const int r = e >> 3, ch = e & 7;
                 const int32_t i = idx[r];
                 const uint8_t* src = i >= 0 ? in + ((int64_t)i * a.cred + c0) * S::ELEM + ch * 16 : in;
-                ptx::cp_async16(a_base + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4), src,
-                                i >= 0 ? 16u : 0u);
+                ptx::cp_async16_hint(a_base + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4),
+                                     src, i >= 0 ? 16u : 0u, keep);
             }
             ptx::cp_async_arrive_noinc(&full[s]);
         }
         ptx::cp_async_wait_all();  // nothing of ours may still land when the CTA ends
-    } else if (warp == 8) {
+    } else if (warp == kTmaWarp) {
         // -------------------------------------------------- weight producer (TMA)
         int issued = 0;
         if (lane == 0) {
@@ -209,7 +213,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             for (int it = first; it < issued; ++it)
                 ptx::mbar_wait(&full[it % STAGES], (it / STAGES) & 1, kWaitNs);
         }
-    } else if (warp == 9 && lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------- MMA issuer
         const uint32_t idesc = ptx::idesc_make(TcKind<T>::fmt, kHalf, BN);
         for (int it = 0; it < n_iter; ++it) {
@@ -238,12 +242,13 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (tid < kEpilogue) {
+    if (tid < kWorkers) {
         const bool waited = ptx::mbar_wait(done, 0, kWaitNs);
         ptx::tc_fence_after();
         const bool aborted = __any_sync(FULL_MASK, !waited || s_ctrl[1] != 0);
-        // warp w reads TMEM lanes 32*(w%4).. of accumulator w/4 (rows 128*(w/4) + ...)
-        const int half = warp >> 2, quarter = warp & 3;
+        // warp w reads TMEM lanes 32*(w%4).. (its lane quarter) of accumulator
+        // (w/4)%2, columns of half w/8 of the tile's BN
+        const int quarter = warp & 3, half = (warp >> 2) & 1, cgrp = warp >> 3;
         const int64_t erow = row0 + half * kHalf + quarter * 32 + lane;
         const bool evalid = erow < a.rows;
         if (aborted) {
@@ -252,7 +257,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             T* out = static_cast<T*>(a.out);
             const T* bias = static_cast<const T*>(a.bias);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = cgrp * (BN / 2); c < (cgrp + 1) * (BN / 2); c += 32) {
                 uint32_t v[32];
                 if (n_iter > 0) {
                     ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * BN + c), v);
@@ -273,14 +278,14 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
                     const uint4* o4 = reinterpret_cast<const uint4*>(o);
                     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                    for (int q = 0; q < (int)(32 * sizeof(T) / 16); ++q) d4[q] = o4[q];
+                    for (int q = 0; q < (int)(32 * sizeof(T) / 16); ++q) __stcs(d4 + q, o4[q]);  // streamed out
                 }
             }
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, S::TMEM_COLS);
     }

@@ -110,6 +110,23 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
                  : "memory");
 }
 
+// L2 policy that keeps lines resident in preference to others (reused data).
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// cp.async with an L2 eviction-priority hint.
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes,
+                                                uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+
 // The mbarrier receives one arrival when every cp.async issued so far by this
 // thread has completed (its expected count must include that arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
