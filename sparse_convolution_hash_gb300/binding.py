@@ -113,7 +113,7 @@ def lib():
             L.spc_conv_wgrad_workspace_size.argtypes = [_i32, _i64, _i64, _i32, _i32, _i32]
             L.spc_conv_wgrad_workspace_size.restype = _sz
             L.spc_conv_wgrad.argtypes = [_p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32, _i32,
-                                         _p, _p, _sz, _p]
+                                         _p, _p, _p, _sz, _p]
             L.spc_conv_wgrad.restype = _i32
             _lib = L
     return _lib
@@ -295,7 +295,8 @@ def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tenso
 
 def spc_conv_wgrad(x: torch.Tensor, dy: torch.Tensor, imap: Optional[torch.Tensor], K: int,
                    precision: int = SPC_PREC_EXACT, out: Optional[torch.Tensor] = None,
-                   ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+                   ws: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None) -> torch.Tensor:
     """dW[k] = sum over pairs of x[imap[k, o]]^T dy[o], float32 [K, cin, cout]."""
     x = _cuda(x, "x")
     dy = _cuda(dy, "dy").to(x.dtype)
@@ -307,6 +308,7 @@ def spc_conv_wgrad(x: torch.Tensor, dy: torch.Tensor, imap: Optional[torch.Tenso
     if ws is None or ws.numel() < nbytes:
         ws = _workspace(nbytes, x.device)
     code = lib().spc_conv_wgrad(_ptr(x), _ptr(dy), _ptr(m), K, x.shape[0], dy.shape[0], cin, cout,
-                                dt, precision, _ptr(dw), _ptr(ws), ws.numel(), _stream(x.device))
+                                dt, precision, _ptr(dw), _ptr(status), _ptr(ws), ws.numel(),
+                                _stream(x.device))
     _check(code, "spc_conv_wgrad")
     return dw

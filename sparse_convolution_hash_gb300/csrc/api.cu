@@ -326,18 +326,28 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     return run_gather(p, dt, st);
 }
 
+namespace {
+size_t wgrad_tc_ws_bytes(int32_t K, int64_t n_out, int32_t cin, int32_t cout)
+{
+    const int splits = wgrad_tc_splits(K, n_out, cin, cout);
+    return sizeof(float) * (size_t)K * (size_t)(cin / 64) * (size_t)(cout / 64) * (size_t)splits * 4096;
+}
+}  // namespace
+
 size_t spc_conv_wgrad_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
                                      int32_t cout, spc_dtype dt)
 {
     (void)n_in;
-    (void)dt;
     if (K < 1 || n_out < 0 || cin < 1 || cout < 1) return 0;
-    return wgrad_ws_bytes(K, n_out, cin, cout);
+    size_t b = wgrad_ws_bytes(K, n_out, cin, cout);
+    if (wgrad_tc_supported(K, cin, cout, dt)) b = std::max(b, wgrad_tc_ws_bytes(K, n_out, cin, cout));
+    return b;
 }
 
 spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, int32_t K,
                           int64_t n_in, int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
-                          spc_precision prec, float* dw, void* ws, size_t ws_bytes, void* stream)
+                          spc_precision prec, float* dw, int32_t* status, void* ws,
+                          size_t ws_bytes, void* stream)
 {
     if (!dtype_ok(dt) || K < 1 || n_in < 0 || n_out < 0 || cin < 1 || cout < 1 || !dw)
         return SPC_ERR_INVALID_ARG;
@@ -348,6 +358,27 @@ spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, in
     if (!imap && n_out > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
     if (ws_bytes < spc_conv_wgrad_workspace_size(K, n_in, n_out, cin, cout, dt) || !ws)
         return SPC_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (imap && n_out > 0 && n_in > 0 && wgrad_tc_supported(K, cin, cout, dt) &&
+        (reinterpret_cast<uintptr_t>(ws) & 15u) == 0) {
+        WgradTcArgs t;
+        t.x = x;
+        t.dy = dy;
+        t.map = imap;
+        t.part = static_cast<float*>(ws);
+        t.status = status;
+        t.n_in = n_in;
+        t.n_out = n_out;
+        t.K = K;
+        t.cin = cin;
+        t.cout = cout;
+        t.splits = wgrad_tc_splits(K, n_out, cin, cout);
+        t.chunk = ceil_div(ceil_div(n_out, t.splits), 128) * 128;
+        t.splits = (int)ceil_div(n_out, t.chunk);
+        spc_status s2 = wgrad_tc(t, dt, st);
+        if (s2 == SPC_OK) return wgrad_reduce(t.part, K, cin, cout, t.splits, dw, st);
+        if (s2 != SPC_ERR_UNSUPPORTED) return s2;
+    }
     WgradArgs a;
     a.x = x;
     a.dy = dy;
@@ -358,7 +389,7 @@ spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, in
     a.K = K;
     a.cin = cin;
     a.cout = cout;
-    return conv_wgrad_simt(a, dt, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+    return conv_wgrad_simt(a, dt, ws, ws_bytes, st);
 }
 
 }  // extern "C"

@@ -253,6 +253,18 @@ size_t wgrad_ws_bytes(int32_t K, int64_t n_out, int32_t cin, int32_t cout)
     return sizeof(float) * (size_t)(K * ctiles * jtiles) * (size_t)wgrad_splits(n_out) * WT * WT;
 }
 
+spc_status wgrad_reduce(const float* part, int32_t K, int32_t cin, int32_t cout, int splits,
+                        float* dw, cudaStream_t st)
+{
+    const int ctiles = (int)ceil_div(cin, WT), jtiles = (int)ceil_div(cout, WT);
+    const int64_t total = (int64_t)K * cin * cout;
+    if (total == 0) return SPC_OK;
+    const int rgrid = (int)std::min<int64_t>(ceil_div(total, kThreads), 4 * sm_count());
+    k_wgrad_reduce<<<rgrid, kThreads, 0, st>>>(part, K, cin, cout, ctiles, jtiles, splits, dw);
+    SPC_LAUNCH_CHECK();
+    return SPC_OK;
+}
+
 spc_status conv_wgrad_simt(const WgradArgs& a, spc_dtype dt, void* ws, size_t ws_bytes,
                            cudaStream_t st)
 {

@@ -39,21 +39,33 @@ namespace spc {
 
 namespace {
 
-constexpr int kHalf = 128;                 // rows per MMA (M)
-constexpr int kRowsPerCta = 2 * kHalf;     // two accumulators share each weight stage
-constexpr int kWorkers = 512;              // warps 0-15: row gathers, then the epilogue
-constexpr int kThreads = kWorkers + 64;    // warp 16: weight TMA; warp 17: TMEM owner, MMA issuer
-constexpr int kTmaWarp = kWorkers / 32, kMmaWarp = kTmaWarp + 1;
+constexpr int kHalf = 128;  // rows per MMA (M)
+#ifndef TC_MT
+#define TC_MT 1
+#endif
+#ifndef TC_NW
+#define TC_NW 8
+#endif
+#ifndef TC_STAGES
+#define TC_STAGES 2
+#endif
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-template <typename T, int BN, int STAGES>
+// MT 128-row MMA tiles per CTA share every weight stage (MT accumulators in
+// TMEM); NW warps gather rows and later run the epilogue; warp NW issues the
+// weight TMA and warp NW + 1 owns TMEM and issues the MMAs.
+template <typename T, int BN, int STAGES, int MT, int NW>
 struct TcShape {
+    static constexpr int kRowsPerCta = MT * kHalf;
+    static constexpr int kWorkers = NW * 32;
+    static constexpr int kThreads = kWorkers + 64;
+    static constexpr int kTmaWarp = NW, kMmaWarp = NW + 1;
     static constexpr int ELEM = (int)sizeof(T);
     static constexpr int CH = 128 / ELEM;  // elements per 128-byte chunk of a row
     static constexpr int A_BYTES = kRowsPerCta * 128;
     static constexpr int B_BYTES = BN * 128;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = MT * BN;
     static size_t smem_bytes(int K)
     {
         return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
@@ -66,11 +78,13 @@ template <> struct TcKind<__half> { static constexpr int kind = 0; static conste
 template <> struct TcKind<__nv_bfloat16> { static constexpr int kind = 0; static constexpr uint32_t fmt = 1; };
 template <> struct TcKind<float> { static constexpr int kind = 1; static constexpr uint32_t fmt = 2; };
 
-template <typename T, int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, int BN, int STAGES, int MT, int NW>
+__global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW>::kThreads, (MT == 1 ? 2 : 1))
 k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 {
-    using S = TcShape<T, BN, STAGES>;
+    using S = TcShape<T, BN, STAGES, MT, NW>;
+    constexpr int kRowsPerCta = S::kRowsPerCta, kWorkers = S::kWorkers;
+    constexpr int kTmaWarp = S::kTmaWarp, kMmaWarp = S::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -88,7 +102,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], kWorkers + 1);  // 512 copy completions + the weight TMA
+            ptx::mbar_init(&full[s], kWorkers + 1);  // one copy completion per worker + the weight TMA
             ptx::mbar_init(&empty[s], 1);
         }
         ptx::mbar_init(done, 1);
@@ -227,14 +241,15 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
-            const uint64_t a0 = ptx::desc_k_sw128(a_base);
-            const uint64_t a1 = ptx::desc_k_sw128(a_base + kHalf * 128);
             const uint64_t bd = ptx::desc_k_sw128(a_base + S::A_BYTES);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per instruction
                 const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
-                ptx::mma<TcKind<T>::kind>(tmem, a0 + 2 * kk, bd + 2 * kk, idesc, acc);
-                ptx::mma<TcKind<T>::kind>(tmem + BN, a1 + 2 * kk, bd + 2 * kk, idesc, acc);
+#pragma unroll
+                for (int h = 0; h < MT; ++h)
+                    ptx::mma<TcKind<T>::kind>(tmem + h * BN,
+                                              ptx::desc_k_sw128(a_base + h * kHalf * 128) + 2 * kk,
+                                              bd + 2 * kk, idesc, acc);
             }
             ptx::mma_commit(&empty[s]);
         }
@@ -247,8 +262,9 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
         ptx::tc_fence_after();
         const bool aborted = __any_sync(FULL_MASK, !waited || s_ctrl[1] != 0);
         // warp w reads TMEM lanes 32*(w%4).. (its lane quarter) of accumulator
-        // (w/4)%2, columns of half w/8 of the tile's BN
-        const int quarter = warp & 3, half = (warp >> 2) & 1, cgrp = warp >> 3;
+        // (w/4)%MT, and column group w/(4 MT) of the tile's BN
+        constexpr int kGroups = NW / (4 * MT), kGroupCols = BN / kGroups;
+        const int quarter = warp & 3, half = (warp >> 2) % MT, cgrp = warp / (4 * MT);
         const int64_t erow = row0 + half * kHalf + quarter * 32 + lane;
         const bool evalid = erow < a.rows;
         if (aborted) {
@@ -257,7 +273,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             T* out = static_cast<T*>(a.out);
             const T* bias = static_cast<const T*>(a.bias);
 #pragma unroll 1
-            for (int c = cgrp * (BN / 2); c < (cgrp + 1) * (BN / 2); c += 32) {
+            for (int c = cgrp * kGroupCols; c < (cgrp + 1) * kGroupCols; c += 32) {
                 uint32_t v[32];
                 if (n_iter > 0) {
                     ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * BN + c), v);
@@ -348,15 +364,16 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int BN, int STAGES>
+template <typename T, int BN, int STAGES, int MT, int NW>
 spc_status launch_tc(const TcArgs& a, cudaStream_t st)
 {
-    using S = TcShape<T, BN, STAGES>;
+    using S = TcShape<T, BN, STAGES, MT, NW>;
+    static_assert(NW % (4 * MT) == 0 && (BN / (NW / (4 * MT))) % 32 == 0, "epilogue split");
     CUtensorMap tb;
     if (!make_tmap<T>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN))
         return SPC_ERR_UNSUPPORTED;
     const size_t smem = S::smem_bytes(a.K);
-    auto kern = k_conv_tc<T, BN, STAGES>;
+    auto kern = k_conv_tc<T, BN, STAGES, MT, NW>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPC_ERR_CUDA;
@@ -366,8 +383,8 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
             return SPC_ERR_UNSUPPORTED;
         configured[dev] = true;
     }
-    dim3 grid((unsigned)ceil_div(a.rows, kRowsPerCta), (unsigned)(a.n_total / BN));
-    kern<<<grid, kThreads, smem, st>>>(a, tb);
+    dim3 grid((unsigned)ceil_div(a.rows, S::kRowsPerCta), (unsigned)(a.n_total / BN));
+    kern<<<grid, S::kThreads, smem, st>>>(a, tb);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }
@@ -375,9 +392,10 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
 template <typename T>
 spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
 {
-    // one CTA per SM; stage counts fill its shared memory
-    if (a.n_total % 128 == 0) return launch_tc<T, 128, 4>(a, st);
-    return launch_tc<T, 64, 4>(a, st);
+    // two CTAs per SM (128-row tiles, 8 gather warps each, two stages each),
+    // so one CTA's prologue and epilogue overlap the other's main loop
+    if (a.n_total % 128 == 0) return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW>(a, st);
+    return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW>(a, st);
 }
 
 }  // namespace

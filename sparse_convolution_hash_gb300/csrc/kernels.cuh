@@ -111,6 +111,24 @@ struct WgradArgs {
     int32_t K, cin, cout;
 };
 size_t wgrad_ws_bytes(int32_t K, int64_t n_out, int32_t cin, int32_t cout);
+// Fixed-order sum of dfilter partials [K x cin/64 x cout/64 tiles][splits][64][64].
+spc_status wgrad_reduce(const float* part, int32_t K, int32_t cin, int32_t cout, int splits,
+                        float* dw, cudaStream_t st);
+
+// Tensor-core dfilter: partial 64 x 64 tiles per (offset, channel tile, row split).
+struct WgradTcArgs {
+    const void* x;
+    const void* dy;
+    const int32_t* map;
+    float* part;            // [tiles][splits][64][64]
+    int32_t* status;
+    int64_t n_in, n_out;
+    int64_t chunk;          // output rows per split (multiple of 128)
+    int32_t K, cin, cout, splits;
+};
+bool wgrad_tc_supported(int32_t K, int32_t cin, int32_t cout, spc_dtype dt);
+int wgrad_tc_splits(int32_t K, int64_t n_out, int32_t cin, int32_t cout);
+spc_status wgrad_tc(const WgradTcArgs& a, spc_dtype dt, cudaStream_t st);
 spc_status conv_wgrad_simt(const WgradArgs& a, spc_dtype dt, void* ws, size_t ws_bytes,
                            cudaStream_t st);
 

@@ -1,0 +1,336 @@
+// wgrad_tc.cu -- dfilter on the tcgen05 tensor cores:
+//   dW[k][c][j] = sum over output rows o with i = imap[k, o] != -1 of x[i][c] dy[o][j].
+//
+// Each CTA owns a group of up to 8 kernel offsets, one 64 x 64 tile of dW
+// (input-channel block x output-channel block) and a fixed chunk of output
+// rows.  For every 128-row slice of its chunk it loads the dy rows once (one
+// 2-D TMA load, 128 x 128 bytes) and, for each offset of its group, gathers the
+// matching x rows through the map with cp.async (rows without a pair are
+// zero-filled, so they add nothing).  The reduction runs over rows, so both
+// operands are MN-major: a gathered row is 64 channels (the M or N index) of
+// one reduction index.  Each offset accumulates into its own 64 x 64 fp32
+// accumulator in tensor memory (8 x 64 columns = all 512).  At the end the
+// CTA writes its partial tiles to the workspace; k_wgrad_reduce sums the
+// chunks in a fixed order, so dW is run-to-run bit-identical.
+//
+// Every barrier wait is bounded (2 s); a wait that runs out sets
+// SPC_ERR_TIMEOUT, the CTA waits (bounded) for its copies and MMAs, frees its
+// tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace spc {
+
+namespace {
+
+constexpr int kRows = 128;      // reduction rows per stage
+constexpr int kGroup = 8;       // offsets per CTA (one accumulator each)
+constexpr int kStages = 4;      // x-gather stages
+constexpr int kWorkers = 256;   // warps 0-7: gathers, then the epilogue
+constexpr int kThreads = kWorkers + 64;  // warp 8: dy TMA; warp 9: TMEM owner, MMA issuer
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kABytes = kRows * 128;  // 64 channels x 2 bytes per row
+constexpr int kBBytes = kRows * 128;
+
+template <typename T> struct TcKindW;
+template <> struct TcKindW<__half> { static constexpr uint32_t fmt = 0; };
+template <> struct TcKindW<__nv_bfloat16> { static constexpr uint32_t fmt = 1; };
+
+// At least 120 KB, so that one CTA (which takes all 512 TMEM columns) owns its SM.
+size_t smem_bytes()
+{
+    const size_t need = 1024 + (size_t)kStages * kABytes + 2 * (size_t)kBBytes + 8 * (2 * kStages + 5) + 64;
+    return need > 120 * 1024 ? need : 120 * 1024;
+}
+
+// MN-major operand, 128-byte swizzle: 8 reduction rows of 128 bytes per atom,
+// atoms stacked every 1024 bytes (stride byte offset).
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;            // leading byte offset: unused (one atom wide)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8 reduction rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* As = smem;                               // [kStages][kABytes]
+    uint8_t* Bs = smem + (size_t)kStages * kABytes;   // [2][kBBytes]
+    uint64_t* afull = reinterpret_cast<uint64_t*>(Bs + 2 * (size_t)kBBytes);
+    uint64_t* aempty = afull + kStages;
+    uint64_t* bfull = aempty + kStages;
+    uint64_t* bempty = bfull + 2;
+    uint64_t* done = bempty + 2;
+    int* s_ctrl = reinterpret_cast<int*>(done + 1);  // abort, tmem
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // which offsets, which dW tile, which rows
+    const int tiles_c = a.cin / 64, tiles_j = a.cout / 64;
+    int t = blockIdx.x;
+    const int jt = t % tiles_j;
+    t /= tiles_j;
+    const int ct = t % tiles_c;
+    const int kg = t / tiles_c;
+    const int k0 = kg * kGroup;
+    const int ng = a.K - k0 < kGroup ? a.K - k0 : kGroup;
+    const int s_split = blockIdx.y;
+    const int64_t o_lo = (int64_t)s_split * a.chunk;
+    const int64_t o_hi = o_lo + a.chunk < a.n_out ? o_lo + a.chunk : a.n_out;
+    const int nrc = o_hi > o_lo ? (int)((o_hi - o_lo + kRows - 1) / kRows) : 0;
+    const int n_iter = nrc * ng;
+    const int c0 = ct * 64, j0 = jt * 64;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&afull[s], kWorkers);
+            ptx::mbar_init(&aempty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bfull[b], 1);
+            ptx::mbar_init(&bempty[b], 1);
+        }
+        ptx::mbar_init(done, 1);
+        s_ctrl[0] = 0;
+        ptx::mbar_init_fence();
+    }
+    if (warp == 8 && lane == 0) ptx::prefetch_tmap(&tma_dy);
+    if (warp == 9) {
+        ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[1]), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = (uint32_t)s_ctrl[1];
+
+    if (tid < kWorkers) {
+        // ------------------------------------------------------ x-row gathers
+        // thread t copies 16-byte chunk (t & 7) of rows 32 j + t / 8 (j < 4); the
+        // map entries of the next stage are loaded while this one is issued
+        const uint8_t* x = static_cast<const uint8_t*>(a.x);
+        const uint64_t keep = ptx::policy_evict_last();
+        const int ch = tid & 7;
+        int32_t idx[4];
+        auto load_idx = [&](int it, int32_t (&v)[4]) {
+            const int rc = it / ng, g = it % ng;
+            const int k = k0 + g;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t o = o_lo + (int64_t)rc * kRows + j * 32 + (tid >> 3);
+                int32_t i = -1;
+                if (it < n_iter && o < o_hi) i = __ldg(a.map + (int64_t)k * a.n_out + o);
+                v[j] = (i >= 0 && i < a.n_in) ? i : -1;
+            }
+        };
+        if (n_iter > 0) load_idx(0, idx);
+        for (int it = 0; it < n_iter; ++it) {
+            const int s = it % kStages;
+            if (it >= kStages && !ptx::mbar_wait(&aempty[s], ((it / kStages) - 1) & 1, kWaitNs)) {
+                atomicExch(&s_ctrl[0], 1);
+                break;
+            }
+            const uint32_t abase = ptx::smem_u32(As + (size_t)s * kABytes);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = j * 32 + (tid >> 3);
+                const int32_t i = idx[j];
+                const uint8_t* src = i >= 0 ? x + ((int64_t)i * a.cin + c0) * sizeof(T) + ch * 16 : x;
+                ptx::cp_async16_hint(abase + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4), src,
+                                     i >= 0 ? 16u : 0u, keep);
+            }
+            ptx::cp_async_arrive_noinc(&afull[s]);
+            int32_t nidx[4];
+            load_idx(it + 1, nidx);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) idx[j] = nidx[j];
+        }
+        ptx::cp_async_wait_all();
+    } else if (warp == 8) {
+        // --------------------------------------------------- dy rows (TMA)
+        if (lane == 0) {
+            int issued = 0;
+            for (int rc = 0; rc < nrc; ++rc) {
+                const int b = rc & 1;
+                if (rc >= 2 && !ptx::mbar_wait(&bempty[b], ((rc >> 1) - 1) & 1, kWaitNs)) {
+                    atomicExch(&s_ctrl[0], 1);
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(&bfull[b], kBBytes);
+                ptx::tma_tile2d(ptx::smem_u32(Bs + (size_t)b * kBBytes), &tma_dy, j0,
+                                (int32_t)(o_lo + (int64_t)rc * kRows), &bfull[b]);
+                ++issued;
+            }
+            const int first = issued > 2 ? issued - 2 : 0;
+            for (int rc = first; rc < issued; ++rc) ptx::mbar_wait(&bfull[rc & 1], (rc >> 1) & 1, kWaitNs);
+        }
+    } else if (warp == 9 && lane == 0) {
+        // ------------------------------------------------------- MMA issuer
+        // M = 64 input channels, N = 64 output channels, both MN-major
+        uint32_t idesc = ptx::idesc_make(TcKindW<T>::fmt, 64, 64);
+        idesc |= 1u << 15;  // A MN-major
+        idesc |= 1u << 16;  // B MN-major
+        bool ok = true;
+        for (int rc = 0; rc < nrc && ok; ++rc) {
+            const int b = rc & 1;
+            if (!ptx::mbar_wait(&bfull[b], (rc >> 1) & 1, kWaitNs)) {
+                ok = false;
+                break;
+            }
+            const uint32_t bbase = ptx::smem_u32(Bs + (size_t)b * kBBytes);
+            for (int g = 0; g < ng; ++g) {
+                const int it = rc * ng + g;
+                const int s = it % kStages;
+                if (!ptx::mbar_wait(&afull[s], (it / kStages) & 1, kWaitNs)) {
+                    ok = false;
+                    break;
+                }
+                ptx::fence_proxy_async_smem();  // the x rows arrived through generic-proxy copies
+                ptx::tc_fence_after();
+                const uint32_t abase = ptx::smem_u32(As + (size_t)s * kABytes);
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk)  // 16 reduction rows (two atoms) per instruction
+                    ptx::mma<0>(tmem + (uint32_t)(g * 64), desc_mn_sw128(abase + kk * 2048),
+                                desc_mn_sw128(bbase + kk * 2048), idesc,
+                                (rc | kk) != 0 ? 1u : 0u);
+                ptx::mma_commit(&aempty[s]);
+            }
+            ptx::mma_commit(&bempty[b]);
+        }
+        if (!ok) atomicExch(&s_ctrl[0], 1);
+        ptx::mma_commit(done);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // M = 64 accumulator rows sit in TMEM lanes 32 q + r (q < 4, r < 16): warp q
+    // of the first four holds rows 16 q .. 16 q + 15 in its lanes 0-15.
+    if (warp < 4) {
+        const bool waited = ptx::mbar_wait(done, 0, kWaitNs);
+        ptx::tc_fence_after();
+        const bool aborted = __any_sync(FULL_MASK, !waited || s_ctrl[0] != 0);
+        if (aborted) {
+            if (tid == 0) set_status(a.status, SPC_ERR_TIMEOUT);
+        } else {
+            const int m = warp * 16 + lane;  // input channel within the tile
+            for (int g = 0; g < ng; ++g) {
+                const int k = k0 + g;
+                const int tile = (k * tiles_c + ct) * tiles_j + jt;
+                float* dst = a.part + ((size_t)tile * a.splits + s_split) * 4096 + (size_t)m * 64;
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 32) {
+                    uint32_t v[32];
+                    if (n_iter > 0) {
+                        ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(g * 64 + c), v);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0u;
+                    }
+                    if (lane < 16) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encoder()
+{
+    static EncodeFn fn = []() -> EncodeFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeFn>(p);
+    }();
+    return fn;
+}
+
+template <typename T>
+spc_status launch(const WgradTcArgs& a, cudaStream_t st)
+{
+    EncodeFn enc = encoder();
+    if (!enc) return SPC_ERR_UNSUPPORTED;
+    CUtensorMap tdy;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.cout, (cuuint64_t)a.n_out};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.cout * sizeof(T)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dtt = sizeof(T) == 2 && TcKindW<T>::fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (enc(&tdy, dtt, 2, const_cast<void*>(a.dy), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SPC_ERR_UNSUPPORTED;
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPC_ERR_CUDA;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(k_wgrad_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes()) != cudaSuccess)
+            return SPC_ERR_UNSUPPORTED;
+        configured[dev] = true;
+    }
+    const int groups = (a.K + kGroup - 1) / kGroup;
+    dim3 grid((unsigned)(groups * (a.cin / 64) * (a.cout / 64)), (unsigned)a.splits);
+    k_wgrad_tc<T><<<grid, kThreads, smem_bytes(), st>>>(a, tdy);
+    SPC_LAUNCH_CHECK();
+    return SPC_OK;
+}
+
+}  // namespace
+
+bool wgrad_tc_supported(int32_t K, int32_t cin, int32_t cout, spc_dtype dt)
+{
+    return (dt == SPC_F16 || dt == SPC_BF16) && K >= 1 && cin % 64 == 0 && cout % 64 == 0;
+}
+
+// Row splits: enough CTAs to fill a GPU of about 160 SMs once.  A fixed target
+// (not the device's SM count) keeps the summation order, and so the result
+// bits, the same on every device.
+int wgrad_tc_splits(int32_t K, int64_t n_out, int32_t cin, int32_t cout)
+{
+    constexpr int64_t kTargetCtas = 160;
+    const int64_t tiles = (int64_t)((K + kGroup - 1) / kGroup) * (cin / 64) * (cout / 64);
+    int64_t s = tiles > 0 ? (kTargetCtas + tiles - 1) / tiles : 1;
+    const int64_t max_s = n_out > 0 ? (n_out + kRows - 1) / kRows : 1;
+    if (s > max_s) s = max_s;
+    return (int)(s < 1 ? 1 : s);
+}
+
+spc_status wgrad_tc(const WgradTcArgs& a, spc_dtype dt, cudaStream_t st)
+{
+    switch (dt) {
+    case SPC_F16: return launch<__half>(a, st);
+    case SPC_BF16: return launch<__nv_bfloat16>(a, st);
+    default: return SPC_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace spc

@@ -126,7 +126,7 @@ def test_argument_errors_return_before_any_work(L):
                             binding.SPC_MAP_TRANSPOSED, ctypes.c_void_p(256), 27, 4, 4, 8, 8, 0, 0,
                             ctypes.c_void_p(256), None, None, 0, None) == E
     assert L.spc_conv_wgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), 27,
-                            4, 4, 8, 8, 2, 0, ctypes.c_void_p(256), None, 0, None) == 8
+                            4, 4, 8, 8, 2, 0, ctypes.c_void_p(256), None, None, 0, None) == 8
     # strided out coords: null n_out / status
     gs = binding.make_geom(3, 2, 1, 1)
     assert L.spc_strided_out_coords(ctypes.c_void_p(256), 4, 1, _i3((8, 8, 8)), ctypes.byref(gs),
