@@ -28,9 +28,10 @@ namespace {
 
 constexpr int kRows = 128;      // reduction rows per stage
 constexpr int kGroup = 8;       // offsets per CTA (one accumulator each)
-constexpr int kStages = 4;      // x-gather stages
-constexpr int kWorkers = 256;   // warps 0-7: gathers, then the epilogue
-constexpr int kThreads = kWorkers + 64;  // warp 8: dy TMA; warp 9: TMEM owner, MMA issuer
+constexpr int kStages = 8;      // x-gather stages (a power of two)
+constexpr int kWorkers = 512;   // warps 0-15: gathers; warps 0-3 then run the epilogue
+constexpr int kThreads = kWorkers + 64;  // warp 16: dy TMA; warp 17: TMEM owner, MMA issuer
+constexpr int kTmaWarp = kWorkers / 32, kMmaWarp = kTmaWarp + 1;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kABytes = kRows * 128;  // 64 channels x 2 bytes per row
 constexpr int kBBytes = kRows * 128;
@@ -105,8 +106,8 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
         s_ctrl[0] = 0;
         ptx::mbar_init_fence();
     }
-    if (warp == 8 && lane == 0) ptx::prefetch_tmap(&tma_dy);
-    if (warp == 9) {
+    if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tma_dy);
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[1]), 512);
         ptx::tmem_relinquish();
     }
@@ -117,47 +118,57 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
 
     if (tid < kWorkers) {
         // ------------------------------------------------------ x-row gathers
-        // thread t copies 16-byte chunk (t & 7) of rows 32 j + t / 8 (j < 4); the
-        // map entries of the next stage are loaded while this one is issued
+        // thread t copies 16-byte chunk (t & 7) of rows 64 j + t / 8 (j < 2).  The
+        // map entries of all offsets of the next 128-row slice are loaded while
+        // the current slice is issued, so no copy waits on a map read.
         const uint8_t* x = static_cast<const uint8_t*>(a.x);
         const uint64_t keep = ptx::policy_evict_last();
         const int ch = tid & 7;
-        int32_t idx[4];
-        auto load_idx = [&](int it, int32_t (&v)[4]) {
-            const int rc = it / ng, g = it % ng;
-            const int k = k0 + g;
+        constexpr int kPer = kRows * 8 / kWorkers;  // rows per thread per stage
+        int32_t cur[kGroup][kPer], nxt[kGroup][kPer];
+        auto load_slice = [&](int rc, int32_t (&v)[kGroup][kPer]) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t o = o_lo + (int64_t)rc * kRows + j * 32 + (tid >> 3);
-                int32_t i = -1;
-                if (it < n_iter && o < o_hi) i = __ldg(a.map + (int64_t)k * a.n_out + o);
-                v[j] = (i >= 0 && i < a.n_in) ? i : -1;
-            }
+            for (int g = 0; g < kGroup; ++g)
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int64_t o = o_lo + (int64_t)rc * kRows + j * (kWorkers / 8) + (tid >> 3);
+                    int32_t i = -1;
+                    if (g < ng && rc < nrc && o < o_hi) i = __ldg(a.map + (int64_t)(k0 + g) * a.n_out + o);
+                    v[g][j] = (i >= 0 && i < a.n_in) ? i : -1;
+                }
         };
-        if (n_iter > 0) load_idx(0, idx);
-        for (int it = 0; it < n_iter; ++it) {
-            const int s = it % kStages;
-            if (it >= kStages && !ptx::mbar_wait(&aempty[s], ((it / kStages) - 1) & 1, kWaitNs)) {
-                atomicExch(&s_ctrl[0], 1);
-                break;
-            }
-            const uint32_t abase = ptx::smem_u32(As + (size_t)s * kABytes);
+        load_slice(0, cur);
+        bool ok = true;
+        for (int rc = 0; rc < nrc && ok; ++rc) {
+            load_slice(rc + 1, nxt);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int r = j * 32 + (tid >> 3);
-                const int32_t i = idx[j];
-                const uint8_t* src = i >= 0 ? x + ((int64_t)i * a.cin + c0) * sizeof(T) + ch * 16 : x;
-                ptx::cp_async16_hint(abase + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4), src,
-                                     i >= 0 ? 16u : 0u, keep);
-            }
-            ptx::cp_async_arrive_noinc(&afull[s]);
-            int32_t nidx[4];
-            load_idx(it + 1, nidx);
+            for (int g = 0; g < kGroup; ++g) {
+                if (g >= ng) break;
+                const int it = rc * ng + g;
+                const int s = it % kStages;
+                if (it >= kStages && !ptx::mbar_wait(&aempty[s], ((it / kStages) - 1) & 1, kWaitNs)) {
+                    atomicExch(&s_ctrl[0], 1);
+                    ok = false;
+                    break;
+                }
+                const uint32_t abase = ptx::smem_u32(As + (size_t)s * kABytes);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) idx[j] = nidx[j];
+                for (int j = 0; j < kPer; ++j) {
+                    const int r = j * (kWorkers / 8) + (tid >> 3);
+                    const int32_t i = cur[g][j];
+                    const uint8_t* src = i >= 0 ? x + ((int64_t)i * a.cin + c0) * sizeof(T) + ch * 16 : x;
+                    ptx::cp_async16_hint(abase + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4),
+                                         src, i >= 0 ? 16u : 0u, keep);
+                }
+                ptx::cp_async_arrive_noinc(&afull[s]);
+            }
+#pragma unroll
+            for (int g = 0; g < kGroup; ++g)
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) cur[g][j] = nxt[g][j];
         }
         ptx::cp_async_wait_all();
-    } else if (warp == 8) {
+    } else if (warp == kTmaWarp) {
         // --------------------------------------------------- dy rows (TMA)
         if (lane == 0) {
             int issued = 0;
@@ -175,7 +186,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
             const int first = issued > 2 ? issued - 2 : 0;
             for (int rc = first; rc < issued; ++rc) ptx::mbar_wait(&bfull[rc & 1], (rc >> 1) & 1, kWaitNs);
         }
-    } else if (warp == 9 && lane == 0) {
+    } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------- MMA issuer
         // M = 64 input channels, N = 64 output channels, both MN-major
         uint32_t idesc = ptx::idesc_make(TcKindW<T>::fmt, 64, 64);
@@ -250,7 +261,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
