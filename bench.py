@@ -342,6 +342,32 @@ class Case:
             h.copy_(d, non_blocking=True)
 
 
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: traffic figures taken from other sources are void."""
+    import glob
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "sparse_convolution_hash_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, phase: str):
+    """DRAM bytes per launch of a phase from the committed ncu capture, or None
+    when the capture was taken on other kernel sources (or is missing)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("src_hash") != kernel_source_hash():
+        return None
+    v = t.get("workloads", {}).get(workload, {}).get(phase)
+    return float(v) if v is not None else None
+
+
 def roofline(p: Phase, ms: float, hbm: float, tc_peak: float, alu_peak: float, dtype: str,
              prec_tf32: bool):
     t_hbm = p.bytes_alg / (hbm * 1e9)
@@ -451,7 +477,7 @@ def run_ours(args, rank, world, local, dist):
         "phases": phases,
         "roofline": {"kernel": f"{dom.name}: {dom.kernels}", "bound": dom_r["bound"],
                      "achieved": dom_r["achieved"], "peak": dom_r["peak"], "unit": dom_r["unit"],
-                     "frac": dom_r["frac"], "traffic": None,
+                     "frac": dom_r["frac"], "traffic": measured_traffic(args.workload, dom.name),
                      "peak_source": f"{peak_src} ({'hbm_gbs burst copy' if dom_r['unit'] == 'GB/s' else 'bf16_tflops burst' if dom_r['bound'] == 'tensor' else 'FP32 lanes x clock'})",
                      "alg_bytes_per_launch": dom.bytes_alg, "alg_flops_per_launch": dom.flops},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",

@@ -54,18 +54,19 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // MT 128-row MMA tiles per CTA share every weight stage (MT accumulators in
 // TMEM); NW warps gather rows and later run the epilogue; warp NW issues the
 // weight TMA and warp NW + 1 owns TMEM and issues the MMAs.
-template <typename T, int BN, int STAGES, int MT, int NW>
+template <typename T, int BN, int STAGES, int MT, int NW, int RB>
 struct TcShape {
     static constexpr int kRowsPerCta = MT * kHalf;
     static constexpr int kWorkers = NW * 32;
     static constexpr int kThreads = kWorkers + 64;
     static constexpr int kTmaWarp = NW, kMmaWarp = NW + 1;
     static constexpr int ELEM = (int)sizeof(T);
-    static constexpr int CH = 128 / ELEM;  // elements per 128-byte chunk of a row
-    static constexpr int A_BYTES = kRowsPerCta * 128;
-    static constexpr int B_BYTES = BN * 128;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = MT * BN;
+    static constexpr int CH = RB / ELEM;   // elements per RB-byte chunk of a row
+    static constexpr int CPR = RB / 16;    // 16-byte pieces per row chunk
+    static constexpr int A_BYTES = kRowsPerCta * RB;
+    static constexpr int B_BYTES = BN * RB;
+    static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int TMEM_COLS = MT * BN <= 32 ? 32 : (MT * BN <= 64 ? 64 : (MT * BN <= 128 ? 128 : (MT * BN <= 256 ? 256 : 512)));
     static size_t smem_bytes(int K)
     {
         return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
@@ -78,11 +79,11 @@ template <> struct TcKind<__half> { static constexpr int kind = 0; static conste
 template <> struct TcKind<__nv_bfloat16> { static constexpr int kind = 0; static constexpr uint32_t fmt = 1; };
 template <> struct TcKind<float> { static constexpr int kind = 1; static constexpr uint32_t fmt = 2; };
 
-template <typename T, int BN, int STAGES, int MT, int NW>
-__global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW>::kThreads, (MT == 1 ? 2 : 1))
+template <typename T, int BN, int STAGES, int MT, int NW, int RB>
+__global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW, RB>::kThreads, (MT == 1 ? 2 : 1))
 k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 {
-    using S = TcShape<T, BN, STAGES, MT, NW>;
+    using S = TcShape<T, BN, STAGES, MT, NW, RB>;
     constexpr int kRowsPerCta = S::kRowsPerCta, kWorkers = S::kWorkers;
     constexpr int kTmaWarp = S::kTmaWarp, kMmaWarp = S::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
@@ -193,13 +194,16 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
             const int32_t* idx = s_idx + ai * kRowsPerCta;
 #pragma unroll
-            for (int j = 0; j < kRowsPerCta * 8 / kWorkers; ++j) {
+            for (int j = 0; j < (kRowsPerCta * S::CPR + kWorkers - 1) / kWorkers; ++j) {
                 const int e = j * kWorkers + tid;
-                const int r = e >> 3, ch = e & 7;
+                if (e >= kRowsPerCta * S::CPR) break;
+                const int r = e / S::CPR, ch = e % S::CPR;
+                // RB-byte swizzle: the piece index XORs with bits 7.. of the row's offset
+                const int sw = ((r * RB) >> 7) & (S::CPR - 1);
                 const int32_t i = idx[r];
                 const uint8_t* src = i >= 0 ? in + ((int64_t)i * a.cred + c0) * S::ELEM + ch * 16 : in;
-                ptx::cp_async16_hint(a_base + (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4),
-                                     src, i >= 0 ? 16u : 0u, keep);
+                ptx::cp_async16_hint(a_base + (uint32_t)r * RB + ((uint32_t)(ch ^ sw) << 4), src,
+                                     i >= 0 ? 16u : 0u, keep);
             }
             ptx::cp_async_arrive_noinc(&full[s]);
         }
@@ -241,14 +245,14 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
-            const uint64_t bd = ptx::desc_k_sw128(a_base + S::A_BYTES);
+            const uint64_t bd = ptx::desc_k_sw<RB>(a_base + S::A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per instruction
+            for (int kk = 0; kk < RB / 32; ++kk) {  // 32 bytes of K per instruction
                 const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
 #pragma unroll
                 for (int h = 0; h < MT; ++h)
                     ptx::mma<TcKind<T>::kind>(tmem + h * BN,
-                                              ptx::desc_k_sw128(a_base + h * kHalf * 128) + 2 * kk,
+                                              ptx::desc_k_sw<RB>(a_base + h * kHalf * RB) + 2 * kk,
                                               bd + 2 * kk, idesc, acc);
             }
             ptx::mma_commit(&empty[s]);
@@ -273,20 +277,23 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
             T* out = static_cast<T*>(a.out);
             const T* bias = static_cast<const T*>(a.bias);
 #pragma unroll 1
-            for (int c = cgrp * kGroupCols; c < (cgrp + 1) * kGroupCols; c += 32) {
-                uint32_t v[32];
+            constexpr int kCols = kGroupCols >= 32 ? 32 : 16;  // TMEM columns per load
+            for (int c = cgrp * kGroupCols; c < (cgrp + 1) * kGroupCols; c += kCols) {
+                uint32_t v[kCols];
                 if (n_iter > 0) {
-                    ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * BN + c), v);
+                    const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * BN + c);
+                    if constexpr (kCols == 32) ptx::tmem_ld32(ta, v);
+                    else ptx::tmem_ld16(ta, v);
                     ptx::tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0u;
+                    for (int j = 0; j < kCols; ++j) v[j] = 0u;
                 }
                 if (evalid) {
                     T* dst = out + erow * a.n_total + n0 + c;
-                    alignas(16) T o[32];
+                    alignas(16) T o[kCols];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < kCols; ++j) {
                         float f = __uint_as_float(v[j]);
                         if (bias) f += elem<T>::to_f32(bias[n0 + c + j]);
                         o[j] = elem<T>::from_f32(f);
@@ -294,7 +301,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
                     const uint4* o4 = reinterpret_cast<const uint4*>(o);
                     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                    for (int q = 0; q < (int)(32 * sizeof(T) / 16); ++q) __stcs(d4 + q, o4[q]);  // streamed out
+                    for (int q = 0; q < (int)(kCols * sizeof(T) / 16); ++q) __stcs(d4 + q, o4[q]);  // streamed out
                 }
             }
         }
@@ -349,31 +356,33 @@ template <> struct TmaType<__half> { static constexpr CUtensorMapDataType v = CU
 template <> struct TmaType<__nv_bfloat16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; };
 template <> struct TmaType<float> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; };
 
-// 2-D row-major [rows, cols] tensor, boxes of 128 bytes x box_rows, 128-byte swizzle.
-template <typename T>
+// 2-D row-major [rows, cols] tensor, boxes of RB bytes x box_rows, RB-byte swizzle.
+template <typename T, int RB>
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows)
 {
     EncodeFn enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * sizeof(T)};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(T)), box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)(RB / sizeof(T)), box_rows};
+    const CUtensorMapSwizzle swz = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : (RB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, TmaType<T>::v, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int BN, int STAGES, int MT, int NW>
+template <typename T, int BN, int STAGES, int MT, int NW, int RB>
 spc_status launch_tc(const TcArgs& a, cudaStream_t st)
 {
-    using S = TcShape<T, BN, STAGES, MT, NW>;
-    static_assert(NW % (4 * MT) == 0 && (BN / (NW / (4 * MT))) % 32 == 0, "epilogue split");
+    using S = TcShape<T, BN, STAGES, MT, NW, RB>;
+    static_assert(NW % (4 * MT) == 0 && (BN / (NW / (4 * MT))) % 16 == 0, "epilogue split");
     CUtensorMap tb;
-    if (!make_tmap<T>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN))
+    if (!make_tmap<T, RB>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN))
         return SPC_ERR_UNSUPPORTED;
     const size_t smem = S::smem_bytes(a.K);
-    auto kern = k_conv_tc<T, BN, STAGES, MT, NW>;
+    auto kern = k_conv_tc<T, BN, STAGES, MT, NW, RB>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPC_ERR_CUDA;
@@ -394,17 +403,36 @@ spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
 {
     // one CTA per SM: 2 x 128-row tiles, 16 gather warps, 4 stages (the
     // fastest of the shapes measured; the gathers are the limiting resource)
-    if (a.n_total % 128 == 0) return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW>(a, st);
-    return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW>(a, st);
+    constexpr int E = (int)sizeof(T);
+    if (a.cred * E % 128 == 0) {
+        if (a.n_total % 128 == 0) return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
+        return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
+    }
+    // narrow rows (32 or 64 bytes): 128-row tiles, 4 gather warps, 8 small stages
+    if (a.cred * E == 64) {
+        if (a.n_total == 16) return launch_tc<T, 16, 8, 1, 4, 64>(a, st);
+        if (a.n_total == 32) return launch_tc<T, 32, 8, 1, 4, 64>(a, st);
+        if (a.n_total % 64 == 0) return launch_tc<T, 64, 8, 1, 4, 64>(a, st);
+    } else if (a.cred * E == 32) {
+        if (a.n_total == 16) return launch_tc<T, 16, 8, 1, 4, 32>(a, st);
+        if (a.n_total == 32) return launch_tc<T, 32, 8, 1, 4, 32>(a, st);
+        if (a.n_total % 64 == 0) return launch_tc<T, 64, 8, 1, 4, 32>(a, st);
+    }
+    return SPC_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
 bool conv_tc_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt, spc_precision prec)
 {
-    if (K < 1 || K > 32 || cout % 64 != 0) return false;
-    if (dt == SPC_F16 || dt == SPC_BF16) return cred % 64 == 0;
-    if (dt == SPC_F32) return prec == SPC_PREC_TF32 && cred % 32 == 0;
+    if (K < 1 || K > 32) return false;
+    const bool wide_n = cout % 64 == 0;
+    if (dt == SPC_F16 || dt == SPC_BF16) {
+        if (cred % 64 == 0) return wide_n;
+        // narrow rows: 16 or 32 channels, N = 16, 32 or a multiple of 64
+        return (cred == 16 || cred == 32) && (cout == 16 || cout == 32 || wide_n);
+    }
+    if (dt == SPC_F32) return prec == SPC_PREC_TF32 && cred % 32 == 0 && wide_n;
     return false;
 }
 

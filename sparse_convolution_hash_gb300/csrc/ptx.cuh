@@ -229,6 +229,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
         : "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle
@@ -241,6 +254,22 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr)
     d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: 8 rows x 128 B
     d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
     d |= (uint64_t)2 << 61;                         // layout: 128-byte swizzle
+    return d;
+}
+
+// K-major operand with rows of RB bytes (32, 64 or 128) in the matching
+// RB-byte swizzle layout: 8-row atoms of 8 * RB bytes stacked densely.
+template <int RB>
+__device__ __forceinline__ uint64_t desc_k_sw(uint32_t saddr)
+{
+    static_assert(RB == 32 || RB == 64 || RB == 128, "row bytes");
+    constexpr uint64_t layout = RB == 128 ? 2 : (RB == 64 ? 4 : 6);
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);        // start address
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused here)
+    d |= (uint64_t)((8 * RB) >> 4) << 32;           // stride byte offset: 8 rows
+    d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
+    d |= layout << 61;                              // swizzle mode
     return d;
 }
 
