@@ -155,10 +155,19 @@ __device__ __forceinline__ int32_t finish_lookup(const unsigned long long* __res
 // mask with 0 beforehand.
 constexpr int kGroup = 3;
 
+// Per-offset table for kernels of at most 32 offsets (precomputed on the host):
+// the cell offset of offset k relative to the query's base cell q*stride - pad,
+// and the matching difference of cell keys, so a neighbour's key is one add.
+constexpr int kMaxTab = 32;
+struct ProbeTab {
+    int32_t dz[kMaxTab], dy[kMaxTab], dx[kMaxTab];
+    long long delta[kMaxTab];
+};
+
 template <bool WRITE_T, bool MIRROR>
 __global__ void __launch_bounds__(kBlock)
-k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, int n_probe,
-            const unsigned long long* __restrict__ slots, int log2b, int vbits,
+k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, ProbeTab tab,
+            int n_probe, const unsigned long long* __restrict__ slots, int log2b, int vbits,
             int32_t* __restrict__ imap, int32_t* __restrict__ imap_t,
             int32_t* __restrict__ pair_count, uint32_t* __restrict__ mask,
             int32_t* __restrict__ status)
@@ -170,7 +179,6 @@ k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, i
     if (threadIdx.x < kGroup) s_cnt[threadIdx.x] = 0;
     __syncthreads();
     const int D = g.in_shape[0], H = g.in_shape[1], W = g.in_shape[2];
-    const int kyx = g.ksize[1] * g.ksize[2];
 
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < nq;
          base += (int64_t)gridDim.x * blockDim.x) {
@@ -188,6 +196,8 @@ k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, i
         const int bz = c.y * g.stride[0] - g.pad[0];
         const int by = c.z * g.stride[1] - g.pad[1];
         const int bx = c.w * g.stride[2] - g.pad[2];
+        // key of the (possibly out-of-grid) base cell; in-grid neighbours add delta
+        const long long kbase = (((long long)c.x * D + bz) * H + by) * W + bx;
 
         unsigned long long key[kGroup], v[kGroup][4];
         uint32_t bucket[kGroup];
@@ -195,11 +205,23 @@ k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, i
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
             const int k = k0 + u;
-            const int kz = k / kyx, ky = (k / g.ksize[2]) % g.ksize[1], kx = k % g.ksize[2];
-            const int z = bz + kz * g.dil[0], y = by + ky * g.dil[1], x = bx + kx * g.dil[2];
-            act[u] = valid && k < n_probe && k != g.centre && z >= 0 && z < D && y >= 0 &&
-                     y < H && x >= 0 && x < W;
-            key[u] = act[u] ? cell_key(c.x, z, y, x, D, H, W) : 0ull;
+            int dz, dy, dx;
+            long long dl;
+            if (k < kMaxTab) {
+                dz = tab.dz[k];
+                dy = tab.dy[k];
+                dx = tab.dx[k];
+                dl = tab.delta[k];
+            } else {  // kernels of more than 32 offsets: decode k on the fly
+                dz = (k / (g.ksize[1] * g.ksize[2])) * g.dil[0];
+                dy = ((k / g.ksize[2]) % g.ksize[1]) * g.dil[1];
+                dx = (k % g.ksize[2]) * g.dil[2];
+                dl = ((long long)dz * H + dy) * W + dx;
+            }
+            const int z = bz + dz, y = by + dy, x = bx + dx;
+            act[u] = valid && k < n_probe && k != g.centre && (unsigned)z < (unsigned)D &&
+                     (unsigned)y < (unsigned)H && (unsigned)x < (unsigned)W;
+            key[u] = act[u] ? (unsigned long long)(kbase + dl) : 0ull;
             bucket[u] = bucket_of(key[u], log2b);
             if (act[u]) load_bucket<false>(slots, bucket[u], v[u]);
         }
@@ -239,12 +261,13 @@ k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, i
 
 template <bool WRITE_T, bool MIRROR>
 void launch_probe(dim3 grid, cudaStream_t st, const int32_t* qcoords, int64_t nq, int64_t n_in,
-                  const ProbeGeom& g, int n_probe, HashTable t, int32_t* imap, int32_t* imap_t,
-                  int32_t* pair_count, uint32_t* mask, int32_t* status)
+                  const ProbeGeom& g, const ProbeTab& tab, int n_probe, HashTable t,
+                  int32_t* imap, int32_t* imap_t, int32_t* pair_count, uint32_t* mask,
+                  int32_t* status)
 {
     k_map_probe<WRITE_T, MIRROR><<<grid, kBlock, 0, st>>>(
-        reinterpret_cast<const int4*>(qcoords), nq, n_in, g, n_probe, t.slots, t.log2_buckets,
-        t.vbits, imap, imap_t, pair_count, mask, status);
+        reinterpret_cast<const int4*>(qcoords), nq, n_in, g, tab, n_probe, t.slots,
+        t.log2_buckets, t.vbits, imap, imap_t, pair_count, mask, status);
 }
 
 }  // namespace
@@ -302,13 +325,26 @@ spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const Pro
     if (mirror && g.K > n_probe)
         SPC_CUDA_TRY(cudaMemsetAsync(imap + (int64_t)n_probe * nq, 0xFF,
                                      sizeof(int32_t) * (size_t)(g.K - n_probe) * (size_t)nq, st));
+    ProbeTab tab;
+    for (int k = 0; k < kMaxTab; ++k) {
+        int dz = 0, dy = 0, dx = 0;
+        if (k < g.K) {
+            dz = (k / (g.ksize[1] * g.ksize[2])) * g.dil[0];
+            dy = ((k / g.ksize[2]) % g.ksize[1]) * g.dil[1];
+            dx = (k % g.ksize[2]) * g.dil[2];
+        }
+        tab.dz[k] = dz;
+        tab.dy[k] = dy;
+        tab.dx[k] = dx;
+        tab.delta[k] = ((long long)dz * g.in_shape[1] + dy) * g.in_shape[2] + dx;
+    }
     const int groups = (int)ceil_div(n_probe, kGroup);
     const int64_t row_blocks = ceil_div(nq, kBlock);
     const int64_t cap = std::max<int64_t>(1, (int64_t)16 * sm_count() / groups);
     dim3 grid((unsigned)std::min<int64_t>(row_blocks, cap), (unsigned)groups);
-    if (imap_t) launch_probe<true, false>(grid, st, qcoords, nq, n_in, g, n_probe, t, imap, imap_t, pair_count, mask, status);
-    else if (mirror) launch_probe<false, true>(grid, st, qcoords, nq, n_in, g, n_probe, t, imap, nullptr, pair_count, mask, status);
-    else launch_probe<false, false>(grid, st, qcoords, nq, n_in, g, n_probe, t, imap, nullptr, pair_count, mask, status);
+    if (imap_t) launch_probe<true, false>(grid, st, qcoords, nq, n_in, g, tab, n_probe, t, imap, imap_t, pair_count, mask, status);
+    else if (mirror) launch_probe<false, true>(grid, st, qcoords, nq, n_in, g, tab, n_probe, t, imap, nullptr, pair_count, mask, status);
+    else launch_probe<false, false>(grid, st, qcoords, nq, n_in, g, tab, n_probe, t, imap, nullptr, pair_count, mask, status);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }
