@@ -49,6 +49,16 @@ constexpr int kHalf = 128;  // rows per MMA (M)
 #ifndef TC_STAGES
 #define TC_STAGES 4
 #endif
+// shape of the narrow-row (16 / 32 channel) instances
+#ifndef TCN_MT
+#define TCN_MT 1
+#endif
+#ifndef TCN_NW
+#define TCN_NW 4
+#endif
+#ifndef TCN_STAGES
+#define TCN_STAGES 8
+#endif
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // MT 128-row MMA tiles per CTA share every weight stage (MT accumulators in
@@ -408,15 +418,15 @@ spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
         if (a.n_total % 128 == 0) return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
         return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
     }
-    // narrow rows (32 or 64 bytes): 128-row tiles, 4 gather warps, 8 small stages
+    // narrow rows (32 or 64 bytes): small stages, many CTAs per SM
     if (a.cred * E == 64) {
-        if (a.n_total == 16) return launch_tc<T, 16, 8, 1, 4, 64>(a, st);
-        if (a.n_total == 32) return launch_tc<T, 32, 8, 1, 4, 64>(a, st);
-        if (a.n_total % 64 == 0) return launch_tc<T, 64, 8, 1, 4, 64>(a, st);
+        if (a.n_total == 16) return launch_tc<T, 16, TCN_STAGES, TCN_MT, TCN_NW, 64>(a, st);
+        if (a.n_total == 32) return launch_tc<T, 32, TCN_STAGES, TCN_MT, TCN_NW, 64>(a, st);
+        if (a.n_total % 64 == 0) return launch_tc<T, 64, TCN_STAGES, TCN_MT, TCN_NW, 64>(a, st);
     } else if (a.cred * E == 32) {
-        if (a.n_total == 16) return launch_tc<T, 16, 8, 1, 4, 32>(a, st);
-        if (a.n_total == 32) return launch_tc<T, 32, 8, 1, 4, 32>(a, st);
-        if (a.n_total % 64 == 0) return launch_tc<T, 64, 8, 1, 4, 32>(a, st);
+        if (a.n_total == 16) return launch_tc<T, 16, TCN_STAGES, TCN_MT, TCN_NW, 32>(a, st);
+        if (a.n_total == 32) return launch_tc<T, 32, TCN_STAGES, TCN_MT, TCN_NW, 32>(a, st);
+        if (a.n_total % 64 == 0) return launch_tc<T, 64, TCN_STAGES, TCN_MT, TCN_NW, 32>(a, st);
     }
     return SPC_ERR_UNSUPPORTED;
 }
