@@ -292,11 +292,21 @@ class Case:
                 "wgrad", lambda: spc.spc_conv_wgrad(self.x, self.dy, self.imap, K, out=self.dw,
                                                     ws=self.wg_ws),
                 "conv", s * n * cin + s * n_out * cout + 4 * P + 4 * K * cin * cout, flops,
-                kernels="k_wgrad_partial, k_wgrad_reduce", launches=2))
+                kernels=("k_wgrad_tc (tcgen05), k_wgrad_reduce"
+                         if self.dtype in ("f16", "bf16") and cin % 64 == 0 and cout % 64 == 0
+                         else "k_wgrad_partial, k_wgrad_reduce"), launches=2))
 
     def fwd_kernel(self, dgrad=False):
+        """Kernels one forward (or dinput) call launches, following the library's
+        dispatch: tcgen05 for 16-bit rows of 16, 32 or a multiple of 64 channels
+        (and tf32), else the SIMT narrow or general gather kernels."""
         cred, co = (self.cout, self.cin) if dgrad else (self.cin, self.cout)
-        if self.dtype in ("f16", "bf16") and cred % 64 == 0 and co % 64 == 0 and self.K <= 32:
+        half = self.dtype in ("f16", "bf16")
+        tc = self.K <= 32 and (
+            (half and cred % 64 == 0 and co % 64 == 0) or
+            (half and cred in (16, 32) and (co in (16, 32) or co % 64 == 0)) or
+            (self.dtype == "f32" and self.prec == self.B.SPC_PREC_TF32 and cred % 32 == 0 and co % 64 == 0))
+        if tc:
             return "k_conv_tc (tcgen05)" + ("" if dgrad else " + k_transpose_w")
         if cred in (8, 16, 32) and co in (8, 16, 32):
             return "k_conv_narrow"
@@ -366,6 +376,57 @@ def measured_traffic(workload: str, phase: str):
         return None
     v = t.get("workloads", {}).get(workload, {}).get(phase)
     return float(v) if v is not None else None
+
+
+# Dominant libspc kernel of each phase, in launch order within one step.
+TRAFFIC_KERNELS = {"outcoords": "k_candidates", "build": "k_map_probe", "fwd": "k_conv_",
+                   "dgrad": "k_conv_", "wgrad": "k_wgrad_(tc|partial)"}
+_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+
+
+def record_traffic(csv_path: str, workload: str, phases):
+    """Store DRAM bytes per launch (read + write) of each phase's dominant kernel
+    from an ncu --csv metrics log into profiles/dram_traffic.json, keyed by the
+    current kernel-source hash.  Launches are assigned to phases in their order
+    within a step (fwd and dgrad both run k_conv_*)."""
+    import csv
+    import re
+
+    per_id = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(l for l in f if l.startswith('"'))]
+    head, body = rows[0], rows[1:]
+    ci = {k: head.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit", "Metric Value")}
+    for r in body:
+        name = r[ci["Metric Name"]]
+        if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        d = per_id.setdefault(int(r[ci["ID"]]), {"kernel": r[ci["Kernel Name"]], "bytes": 0.0})
+        d["bytes"] += float(r[ci["Metric Value"]].replace(",", "")) * _UNITS.get(r[ci["Metric Unit"]], 1)
+    seq = [(ph, TRAFFIC_KERNELS[ph]) for ph in phases if ph in TRAFFIC_KERNELS]
+    got = {ph: [] for ph, _ in seq}
+    j = 0
+    for i in sorted(per_id):
+        if not seq:
+            break
+        ph, pat = seq[j]
+        if re.search(pat, per_id[i]["kernel"]):
+            got[ph].append(per_id[i]["bytes"])
+            j = (j + 1) % len(seq)
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        t = {}
+    if t.get("src_hash") != kernel_source_hash():
+        t = {"src_hash": kernel_source_hash(), "workloads": {}}
+    t["note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch of each phase's "
+                 "dominant kernel, mean over the captured launches (ncu, cold caches)")
+    t["workloads"][workload] = {ph: round(sum(v) / len(v)) for ph, v in got.items() if v}
+    with open(path, "w") as f:
+        json.dump(t, f, indent=1, sort_keys=True)
+    print(json.dumps({workload: t["workloads"][workload]}))
 
 
 def roofline(p: Phase, ms: float, hbm: float, tc_peak: float, alu_peak: float, dtype: str,
@@ -583,7 +644,16 @@ def main():
     ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store the DRAM bytes of an ncu metrics log of this workload and exit")
     args = ap.parse_args()
+    if args.record_traffic:
+        w = scenes.workload(args.workload)
+        phases = (["build"] if w["subm"] and w["k"] > 1 else []) + \
+                 ([] if w["subm"] else ["outcoords", "build"]) + ["fwd"] + \
+                 (["dgrad", "wgrad"] if w.get("train") else [])
+        record_traffic(args.record_traffic, args.workload, phases)
+        return
     args.warmup = max(args.warmup, 3)
     rank, world, local, dist = dist_setup()
     if args.impl == "reference":
