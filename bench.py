@@ -298,9 +298,12 @@ class Case:
 
     def fwd_kernel(self, dgrad=False):
         """Kernels one forward (or dinput) call launches, following the library's
-        dispatch: tcgen05 for 16-bit rows of 16, 32 or a multiple of 64 channels
-        (and tf32), else the SIMT narrow or general gather kernels."""
+        dispatch: the CUDA-core narrow kernel when both widths are 8, 16 or 32,
+        tcgen05 for 16-bit rows of 16, 32 or a multiple of 64 channels (and
+        tf32), else the general CUDA-core gather kernel."""
         cred, co = (self.cout, self.cin) if dgrad else (self.cin, self.cout)
+        if cred in (8, 16, 32) and co in (8, 16, 32) and (cred, co) not in ((8, 32), (32, 8)):
+            return "k_conv_narrow"
         half = self.dtype in ("f16", "bf16")
         tc = self.K <= 32 and (
             (half and cred % 64 == 0 and co % 64 == 0) or
@@ -308,8 +311,6 @@ class Case:
             (self.dtype == "f32" and self.prec == self.B.SPC_PREC_TF32 and cred % 32 == 0 and co % 64 == 0))
         if tc:
             return "k_conv_tc (tcgen05)" + ("" if dgrad else " + k_transpose_w")
-        if cred in (8, 16, 32) and co in (8, 16, 32):
-            return "k_conv_narrow"
         return "k_gather_gemm_simt"
 
     def conv_flops(self):
@@ -378,17 +379,19 @@ def measured_traffic(workload: str, phase: str):
     return float(v) if v is not None else None
 
 
-# Dominant libspc kernel of each phase, in launch order within one step.
-TRAFFIC_KERNELS = {"outcoords": "k_candidates", "build": "k_map_probe", "fwd": "k_conv_",
-                   "dgrad": "k_conv_", "wgrad": "k_wgrad_(tc|partial)"}
 _UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
 
 
 def record_traffic(csv_path: str, workload: str, phases):
-    """Store DRAM bytes per launch (read + write) of each phase's dominant kernel
-    from an ncu --csv metrics log into profiles/dram_traffic.json, keyed by the
-    current kernel-source hash.  Launches are assigned to phases in their order
-    within a step (fwd and dgrad both run k_conv_*)."""
+    """Store the DRAM bytes (read + write) of one call of each phase -- the sum
+    over the libspc kernels the phase launches -- from an ncu --csv metrics log
+    into profiles/dram_traffic.json, keyed by the current kernel-source hash.
+
+    Kernels are grouped by phase: out-coords (candidates, radix sort, unique),
+    build (table clear, insert, map probe), conv (weight transpose + gather
+    kernels; with a backward pass the conv launches alternate forward, dinput)
+    and dfilter.  A phase's bytes are its kernels' bytes divided by the number
+    of its calls (counted by one anchor kernel per phase)."""
     import csv
     import re
 
@@ -403,16 +406,30 @@ def record_traffic(csv_path: str, workload: str, phases):
             continue
         d = per_id.setdefault(int(r[ci["ID"]]), {"kernel": r[ci["Kernel Name"]], "bytes": 0.0})
         d["bytes"] += float(r[ci["Metric Value"]].replace(",", "")) * _UNITS.get(r[ci["Metric Unit"]], 1)
-    seq = [(ph, TRAFFIC_KERNELS[ph]) for ph in phases if ph in TRAFFIC_KERNELS]
-    got = {ph: [] for ph, _ in seq}
-    j = 0
-    for i in sorted(per_id):
-        if not seq:
-            break
-        ph, pat = seq[j]
-        if re.search(pat, per_id[i]["kernel"]):
-            got[ph].append(per_id[i]["bytes"])
-            j = (j + 1) % len(seq)
+    launches = [per_id[i] for i in sorted(per_id)]
+
+    def k(pattern):
+        return [d for d in launches if re.search(r"::" + pattern, d["kernel"])]
+
+    def per_call(group, anchor):
+        n = len(k(anchor))
+        return sum(d["bytes"] for d in group) / n if n else None
+
+    got = {}
+    if "outcoords" in phases:
+        got["outcoords"] = per_call(k(r"k_(candidates|radix|scan|unique)"), r"k_candidates")
+    if "build" in phases:
+        got["build"] = per_call(k(r"k_(hash_clear|hash_insert|map_probe)"), r"k_map_probe")
+    conv = k(r"k_(conv_|gather_gemm)")
+    fwd, dgr = (conv[0::2], conv[1::2]) if "dgrad" in phases else (conv, [])
+    tr = k(r"k_transpose_w")
+    if fwd:
+        got["fwd"] = sum(d["bytes"] for d in fwd) / len(fwd) + (
+            sum(d["bytes"] for d in tr) / len(tr) if tr else 0.0)
+    if dgr:
+        got["dgrad"] = sum(d["bytes"] for d in dgr) / len(dgr)
+    if "wgrad" in phases:
+        got["wgrad"] = per_call(k(r"k_wgrad"), r"k_wgrad_(tc|partial)")
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -421,9 +438,9 @@ def record_traffic(csv_path: str, workload: str, phases):
         t = {}
     if t.get("src_hash") != kernel_source_hash():
         t = {"src_hash": kernel_source_hash(), "workloads": {}}
-    t["note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch of each phase's "
-                 "dominant kernel, mean over the captured launches (ncu, cold caches)")
-    t["workloads"][workload] = {ph: round(sum(v) / len(v)) for ph, v in got.items() if v}
+    t["note"] = ("DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one call of each "
+                 "phase, summed over the kernels it launches; ncu, cold caches")
+    t["workloads"][workload] = {ph: round(v) for ph, v in got.items() if v is not None}
     with open(path, "w") as f:
         json.dump(t, f, indent=1, sort_keys=True)
     print(json.dumps({workload: t["workloads"][workload]}))

@@ -249,7 +249,11 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
     p.mirror = 0;
     p.transpose_w = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (n_out > 0 && conv_tc_supported(cin, cout, K, dt, prec) && aligned16(x) && aligned16(y)) {
+    // channel widths of 8 / 16 / 32 on both sides: the latency-oriented CUDA-core
+    // kernel (a row has few neighbours on sparse scenes; a tensor-core tile
+    // would mostly multiply zero-filled rows)
+    const bool narrow = conv_narrow_supported(cin, cout, K, dt);
+    if (n_out > 0 && !narrow && conv_tc_supported(cin, cout, K, dt, prec) && aligned16(x) && aligned16(y)) {
         const size_t wbytes = conv_tc_weight_bytes(K, cin, cout, dt);
         if (!ws || ws_bytes < wbytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
             return SPC_ERR_WORKSPACE;
@@ -304,7 +308,8 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     p.mirror = (kind == SPC_MAP_SUBM_MIRROR) ? 1 : 0;
     p.transpose_w = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (n_in > 0 && conv_tc_supported(cout, cin, K, dt, prec) && aligned16(dy) && aligned16(dx)) {
+    const bool narrow = conv_narrow_supported(cout, cin, K, dt);
+    if (n_in > 0 && !narrow && conv_tc_supported(cout, cin, K, dt, prec) && aligned16(dy) && aligned16(dx)) {
         // W[k] is [Cin][Cout]: already the [N][K] K-major operand of dx = dy W[k]^T
         TcArgs a;
         a.in = dy;

@@ -1,14 +1,17 @@
 // conv_narrow.cu -- gathered conv for narrow channels (Cin, Cout in {8, 16, 32}).
 //
 // Narrow layers move far more bytes than they compute (a 16 -> 16 pair is 256
-// multiply-adds on a 32-byte row), so this path is laid out for memory, not
-// for tensor cores: one thread owns one output row and keeps its Cout fp32
-// accumulators in registers; the weight tensor is converted to fp32 once per
-// persistent block and kept in shared memory.  A warp walks the union of its
-// rows' offset masks in a warp-uniform order, so all lanes working on offset k
-// read the same W[k] words (shared-memory broadcast), and only lanes whose row
-// has a neighbour at k read the map entry and gather the neighbour's row
-// (16-byte vector loads).  Rows are written once, with vector stores.
+// multiply-adds on a 32-byte row), and on sparse scenes most rows have only a
+// few neighbours, so this path is laid out for latency, not for tensor cores:
+// one thread owns one output row and keeps its Cout fp32 accumulators in
+// registers; the weight tensor is converted to fp32 once per persistent block
+// and kept in shared memory (each offset's slice padded by 16 bytes, so lanes
+// reading different offsets' slices spread over the banks).  A thread walks
+// only its own row's offset mask, a few offsets at a time: their map entries
+// are loaded together, then their neighbours' rows (16-byte vector loads),
+// then the multiply-adds run.  A row with at most that many neighbours costs
+// two dependent memory round trips.  Rows are written once, with vector
+// stores.  Blocks are sized so that the whole grid is resident at once.
 //
 // The same kernel computes dinput with the transposed weight slice and the
 // transposed map (or the submanifold map read through its offset mirror, in
@@ -34,7 +37,7 @@ __device__ __forceinline__ void fma_row(float (&acc)[COUT], const RowVec<T, CRED
 {
     const T* xe = reinterpret_cast<const T*>(xv.w);
     const float4* w4 = reinterpret_cast<const float4*>(wk);
-#pragma unroll
+#pragma unroll 4
     for (int c = 0; c < CRED; ++c) {
         const float xc = elem<T>::to_f32(xe[c]);
 #pragma unroll
@@ -56,15 +59,64 @@ __device__ __forceinline__ void load_row(RowVec<T, N>& v, const T* __restrict__ 
     for (int q = 0; q < RowVec<T, N>::kWords; ++q) v.w[q] = __ldg(src + q);
 }
 
+// fp32 words between consecutive offsets' weight slices in shared memory
+template <int CRED, int COUT>
+constexpr int kSliceStride = CRED * COUT + 4;
+
 template <typename T, int CRED, int COUT>
-__global__ void __launch_bounds__(kThreads) k_conv_narrow(GatherGemm p)
+constexpr int kNarrowBatch = CRED * (int)sizeof(T) >= 64 ? 1 : (CRED * (int)sizeof(T) >= 32 ? 2 : 4);
+
+// Up to kBatch of the offsets left in m (lowest first, removed from m): their
+// map entries, then their neighbours' rows, all loads in flight together.
+template <typename T, int CRED, int kBatch>
+__device__ __forceinline__ void load_batch(uint32_t& m, const GatherGemm& p, int64_t r, int (&ks)[kBatch],
+                                           int32_t (&idx)[kBatch], RowVec<T, CRED> (&xv)[kBatch])
 {
-    // offsets whose map and row loads are in flight together (about 32 registers of rows)
-    constexpr int kRowRegs = CRED * (int)sizeof(T) / 4;
-    constexpr int kBatch = kRowRegs >= 32 ? 1 : (kRowRegs >= 16 ? 2 : 4);
-    extern __shared__ __align__(16) float s_w[];  // [K][CRED][COUT] fp32, then bias [COUT]
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+        ks[b] = m ? __ffs(m) - 1 : -1;
+        m &= m - 1;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+        idx[b] = -1;
+        if (ks[b] >= 0) {
+            const int mk = p.mirror ? p.K - 1 - ks[b] : ks[b];
+            idx[b] = p.map ? __ldcs(p.map + (int64_t)mk * p.rows + r) : (int32_t)r;
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+        if (idx[b] >= 0) load_row(xv[b], static_cast<const T*>(p.in), idx[b]);
+}
+
+template <typename T, int CRED, int COUT>
+__global__ void __launch_bounds__(kThreads, (COUT <= 16 ? 4 : 2)) k_conv_narrow(GatherGemm p)
+{
+    // offsets whose map entries and rows are in flight together
+    constexpr int kBatch = kNarrowBatch<T, CRED, COUT>;
+    constexpr int kStr = kSliceStride<CRED, COUT>;
+    extern __shared__ __align__(16) float s_w[];  // [K][kStr] fp32 ([CRED][COUT] + pad), then bias [COUT]
     const T* __restrict__ in = static_cast<const T*>(p.in);
     const int K = p.K;
+    const uint32_t kmask = K >= 32 ? 0xffffffffu : ((1u << K) - 1u);
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+
+    // The first row's mask, map entries and neighbour rows are requested before
+    // the block stages its weights, so the two latencies overlap.
+    uint32_t m = 0;
+    int ks[kBatch];
+    int32_t idx[kBatch];
+    RowVec<T, CRED> xv[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) idx[b] = -1;
+    if (p.mask && r < p.rows) {
+        m = __ldcs(p.mask + r);  // read once: evict first
+        if (p.mirror) m = __brev(m) >> (32 - K);
+        m &= kmask;
+        load_batch<T, CRED, kBatch>(m, p, r, ks, idx, xv);
+    }
     {
         // weights: 16-byte vector loads in global order, converted to fp32
         constexpr int kPer = 16 / (int)sizeof(T);
@@ -85,92 +137,65 @@ __global__ void __launch_bounds__(kThreads) k_conv_narrow(GatherGemm p)
 #pragma unroll
                 for (int t = 0; t < kPer; ++t) {
                     const int g = v * kPer + t;  // global element index
-                    int dst = g;
-                    if (p.transpose_w) {  // global [K][COUT][CRED] -> shared [K][CRED][COUT]
-                        const int k = g / (CRED * COUT), a = (g / CRED) % COUT, b = g % CRED;
-                        dst = (k * CRED + b) * COUT + a;
+                    const int k = g / (CRED * COUT);
+                    int a = (g / COUT) % CRED, b = g % COUT;  // [K][CRED][COUT] order
+                    if (p.transpose_w) {  // global [K][COUT][CRED]
+                        a = g % CRED;
+                        b = (g / CRED) % COUT;
                     }
-                    s_w[dst] = elem<T>::to_f32(e[t]);
+                    s_w[k * kStr + a * COUT + b] = elem<T>::to_f32(e[t]);
                 }
             }
         }
     }
-    float* s_bias = s_w + (size_t)K * CRED * COUT;
+    float* s_bias = s_w + (size_t)K * kStr;
     for (int j = threadIdx.x; j < COUT; j += blockDim.x)
         s_bias[j] = p.bias ? elem<T>::to_f32(static_cast<const T*>(p.bias)[j]) : 0.f;
     __syncthreads();
 
-    const uint32_t kmask = K >= 32 ? 0xffffffffu : ((1u << K) - 1u);
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < p.rows; base += step) {
-        const int64_t r = base + threadIdx.x;
-        const bool valid = r < p.rows;
+    for (bool first = true; r < p.rows; r += step, first = false) {
         float acc[COUT];
 #pragma unroll
         for (int j = 0; j < COUT; ++j) acc[j] = s_bias[j];
 
         if (p.mask) {
-            uint32_t m = 0;
-            if (valid) {
-                m = p.mask[r];
+            if (!first) {
+                m = __ldcs(p.mask + r);
                 if (p.mirror) m = __brev(m) >> (32 - K);
                 m &= kmask;
+                load_batch<T, CRED, kBatch>(m, p, r, ks, idx, xv);
             }
-            uint32_t todo = __reduce_or_sync(FULL_MASK, m);
-            while (todo) {
-                // take up to kBatch offsets of the warp's union (warp-uniform)
-                int ks[kBatch];
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    ks[b] = todo ? __ffs(todo) - 1 : -1;
-                    todo &= todo - 1;
-                }
-                int32_t idx[kBatch];
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    idx[b] = -1;
-                    if (ks[b] >= 0 && ((m >> ks[b]) & 1u)) {
-                        const int mk = p.mirror ? K - 1 - ks[b] : ks[b];
-                        idx[b] = p.map ? p.map[(int64_t)mk * p.rows + r] : (int32_t)r;
-                    }
-                }
-                RowVec<T, CRED> xv[kBatch];
+            while (true) {
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b)
-                    if (idx[b] >= 0) load_row(xv[b], in, idx[b]);
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b)
-                    if (idx[b] >= 0) fma_row<T, CRED, COUT>(acc, xv[b], s_w + (size_t)ks[b] * CRED * COUT);
+                    if (idx[b] >= 0) fma_row<T, CRED, COUT>(acc, xv[b], s_w + (size_t)ks[b] * kStr);
+                if (!m) break;
+                load_batch<T, CRED, kBatch>(m, p, r, ks, idx, xv);
             }
         } else {
             for (int k = 0; k < K; ++k) {
-                int32_t i = -1;
-                if (valid) {
-                    const int mk = p.mirror ? K - 1 - k : k;
-                    i = p.map ? p.map[(int64_t)mk * p.rows + r] : (int32_t)r;
-                }
+                const int mk = p.mirror ? K - 1 - k : k;
+                const int32_t i = p.map ? p.map[(int64_t)mk * p.rows + r] : (int32_t)r;
                 if (i < 0) continue;
-                RowVec<T, CRED> xv;
-                load_row(xv, in, i);
-                fma_row<T, CRED, COUT>(acc, xv, s_w + (size_t)k * CRED * COUT);
+                RowVec<T, CRED> xr;
+                load_row(xr, in, i);
+                fma_row<T, CRED, COUT>(acc, xr, s_w + (size_t)k * kStr);
             }
         }
-        if (valid) {
-            RowVec<T, COUT> ov;
-            T* oe = reinterpret_cast<T*>(ov.w);
+        RowVec<T, COUT> ov;
+        T* oe = reinterpret_cast<T*>(ov.w);
 #pragma unroll
-            for (int j = 0; j < COUT; ++j) oe[j] = elem<T>::from_f32(acc[j]);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + r * COUT);
+        for (int j = 0; j < COUT; ++j) oe[j] = elem<T>::from_f32(acc[j]);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + r * COUT);
 #pragma unroll
-            for (int q = 0; q < RowVec<T, COUT>::kWords; ++q) dst[q] = ov.w[q];
-        }
+        for (int q = 0; q < RowVec<T, COUT>::kWords; ++q) __stcs(dst + q, ov.w[q]);  // streamed out
     }
 }
 
 template <typename T, int CRED, int COUT>
 spc_status launch(const GatherGemm& p, cudaStream_t st)
 {
-    const size_t smem = sizeof(float) * ((size_t)p.K * CRED * COUT + COUT);
+    const size_t smem = sizeof(float) * ((size_t)p.K * kSliceStride<CRED, COUT> + COUT);
     auto kern = k_conv_narrow<T, CRED, COUT>;
     if (smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -224,7 +249,7 @@ bool conv_narrow_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt)
     if (cred == 8 && cout == 32) return false;
     if (cred == 32 && cout == 8) return false;
     // fp32 weights of all offsets must fit in shared memory
-    if ((size_t)K * cred * cout * sizeof(float) > 200 * 1024) return false;
+    if ((size_t)K * (cred * cout + 4) * sizeof(float) > 200 * 1024) return false;
     (void)dt;
     return true;
 }

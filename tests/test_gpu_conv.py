@@ -48,7 +48,8 @@ def subm_case(coords, batch, shape, cin, cout, dtype, ks=3, seed=0, bias=True):
                                         (2100, 64, 128), (900, 128, 96), (640, 32, 32),
                                         (333, 16, 32), (1029, 32, 16), (515, 8, 16),
                                         (1000, 128, 128), (3000, 64, 64), (700, 192, 64),
-                                        (513, 64, 256), (129, 128, 64)])
+                                        (513, 64, 256), (129, 128, 64), (600, 16, 64),
+                                        (450, 32, 128)])
 def test_subm_small_full(dtype, prec, n, cin, cout):
     g = np.random.default_rng(n)
     batch, shape = 2, (12, 11, 13)
