@@ -127,16 +127,24 @@ spc_status spc_build_indice_map(const int32_t* coords, int64_t n_in, int32_t bat
     if (!ws || ws_bytes < spc_indice_map_workspace_size(n_in)) return SPC_ERR_WORKSPACE;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    SPC_CUDA_TRY(cudaMemsetAsync(pair_count, 0, sizeof(int32_t) * (size_t)K, st));
-    if (imap_t && n_in > 0) SPC_CUDA_TRY(cudaMemsetAsync(imap_t, 0xFF, sizeof(int32_t) * (size_t)(K * n_in), st));
-    if (n_out == 0 && n_in == 0) return SPC_OK;
-
     HashTable t;
     t.slots = static_cast<unsigned long long*>(ws);
     t.log2_buckets = ceil_log2((uint64_t)hash_slots_for(n_in)) - 2;
     t.vbits = vbits;
-    spc_status s = hash_clear(t, st);
+    // one launch prepares every buffer: zero pair counts, -1 transposed map,
+    // empty table, zero mask, -1 for the mirrored rows of a submanifold map
+    FillList fl;
+    int nf = 0;
+    fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(pair_count), K, 0u};
+    if (imap_t && n_in > 0) fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(imap_t), (int64_t)K * n_in, 0xFFFFFFFFu};
+    if (n_out > 0 || n_in > 0) fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(t.slots), (int64_t)8 << t.log2_buckets, 0xFFFFFFFFu};
+    if (mask && n_out > 0) fl.r[nf++] = FillRegion{mask, n_out, 0u};
+    if (n_out > 0 && probe_mirror(pg, imap_t != nullptr))
+        fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(imap + (int64_t)(pg.centre + 1) * n_out),
+                                (int64_t)(K - pg.centre - 1) * n_out, 0xFFFFFFFFu};
+    spc_status s = build_init(fl, nf, st);
     if (s != SPC_OK) return s;
+    if (n_out == 0 && n_in == 0) return SPC_OK;
     s = hash_insert(coords, n_in, batch, in_shape, t, status, st);
     if (s != SPC_OK) return s;
     return map_probe(out_coords, n_out, n_in, pg, t, imap, imap_t, pair_count, mask, status, st);

@@ -13,6 +13,8 @@
 // 128-byte rows of imap, and the per-offset pair counts are one ballot per
 // offset.  Inserts claim the first empty slot with a 64-bit CAS.  Every probe
 // loop is bounded; exceeding the bound sets SPC_ERR_TABLE_FULL.
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace spc {
@@ -28,19 +30,51 @@ __device__ __forceinline__ uint32_t bucket_of(unsigned long long key, int log2b)
     return log2b == 0 ? 0u : (uint32_t)(h >> (64 - log2b));
 }
 
+// Slot of the bucket an insert tries first (bits below the bucket index).
+__device__ __forceinline__ int home_slot(unsigned long long key)
+{
+    return (int)(((key * 0x9E3779B97F4A7C15ull) >> 30) & 3u);
+}
+
 __device__ __forceinline__ unsigned long long cell_key(int b, int z, int y, int x, int D, int H,
                                                        int W)
 {
     return (((unsigned long long)b * D + (unsigned)z) * H + (unsigned)y) * W + (unsigned)x;
 }
 
-__global__ void __launch_bounds__(kBlock)
-k_hash_clear(unsigned long long* __restrict__ slots, int64_t n)
+// Fills every region of the list with its 32-bit pattern: the empty table, the
+// zeroed pair counts and mask, and the map rows that start at -1.  One launch
+// instead of a memset per buffer.  The 16-byte-aligned bodies of the regions
+// form one index space that the grid strides over; the first threads also
+// write each region's unaligned head and tail words.
+__global__ void __launch_bounds__(kBlock) k_build_init(FillList L, int n)
 {
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t start[6];  // first 16-byte word of each region's body in the joint index space
+    int64_t head[5];
+    start[0] = 0;
+    for (int i = 0; i < 5; ++i) {
+        const FillRegion& f = L.r[i];
+        const int64_t nn = i < n ? f.n : 0;
+        head[i] = nn > 0 ? std::min<int64_t>(nn, (int64_t)((16 - (reinterpret_cast<uintptr_t>(f.p) & 15)) & 15) / 4) : 0;
+        start[i + 1] = start[i] + (nn - head[i]) / 4;
+    }
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t0 < 6 * 5) {  // heads (words 0..2) and tails (3..5) of region t0 / 6
+        const int i = (int)(t0 / 6), w = (int)(t0 % 6);
+        if (i < n && L.r[i].n > 0) {
+            const FillRegion& f = L.r[i];
+            const int64_t body_end = head[i] + (start[i + 1] - start[i]) * 4;
+            const int64_t at = w < 3 ? w : body_end + (w - 3);
+            if ((w < 3 && at < head[i]) || (w >= 3 && at < f.n)) f.p[at] = f.v;
+        }
+    }
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    ulonglong2* s2 = reinterpret_cast<ulonglong2*>(slots);
-    for (; i < n / 2; i += stride) s2[i] = make_ulonglong2(EMPTY, EMPTY);
+    int i = 0;
+    for (int64_t j = t0; j < start[5]; j += stride) {
+        while (j >= start[i + 1]) ++i;
+        const FillRegion& f = L.r[i];
+        reinterpret_cast<uint4*>(f.p + head[i])[j - start[i]] = make_uint4(f.v, f.v, f.v, f.v);
+    }
 }
 
 // Reads one 32-byte bucket (four slots) with two 16-byte loads.
@@ -85,6 +119,18 @@ k_hash_insert(const int4* __restrict__ coords, int64_t n, int32_t batch, int D, 
         const unsigned long long key = cell_key(c.x, c.y, c.z, c.w, D, H, W);
         const unsigned long long entry = (key << vbits) | (unsigned long long)r;
         uint32_t bucket = bucket_of(key, log2b);
+        // First try the key's home slot in its bucket with a CAS and no read: at
+        // load factor <= 1/2 it is usually free, and a taken slot returns its
+        // occupant (a duplicate shows here too).  Lookups scan whole buckets, so
+        // any free slot of the first non-full bucket is a valid place.
+        {
+            const unsigned long long old = atomicCAS(&slots[(size_t)bucket * 4 + home_slot(key)], EMPTY, entry);
+            if (old == EMPTY) continue;
+            if ((old >> vbits) == key) {
+                set_status(status, SPC_ERR_DUPLICATE);
+                continue;
+            }
+        }
         uint32_t it = 0;
         for (; it < bound; ++it) {
             unsigned long long v[4];
@@ -292,13 +338,22 @@ bool hash_keys_fit(int64_t cells, int vbits)
     return (unsigned long long)cells <= ((1ull << kbits) - 1ull);
 }
 
-spc_status hash_clear(HashTable t, cudaStream_t st)
+spc_status build_init(const FillList& L, int n, cudaStream_t st)
 {
-    const int64_t n = 4ll << t.log2_buckets;
-    const int grid = (int)std::min<int64_t>(ceil_div(n / 2, kBlock), 4 * sm_count());
-    k_hash_clear<<<grid, kBlock, 0, st>>>(t.slots, n);
+    int64_t words = 0;
+    for (int i = 0; i < n; ++i) words += std::max<int64_t>(L.r[i].n, 0);
+    if (n == 0 || words == 0) return SPC_OK;
+    FillList l = L;
+    for (int i = n; i < 5; ++i) l.r[i] = FillRegion{nullptr, 0, 0u};
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ceil_div(words / 4 + 30, kBlock), 4 * sm_count()));
+    k_build_init<<<grid, kBlock, 0, st>>>(l, n);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
+}
+
+bool probe_mirror(const ProbeGeom& g, bool with_transpose)
+{
+    return g.centre >= 0 && !with_transpose && g.K == 2 * g.centre + 1;
 }
 
 spc_status hash_insert(const int32_t* coords, int64_t n, int32_t batch, const int32_t shape[3],
@@ -318,13 +373,10 @@ spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const Pro
                      uint32_t* mask, int32_t* status, cudaStream_t st)
 {
     if (nq == 0) return SPC_OK;
-    // submanifold maps (centre >= 0, odd kernels) are probed for k <= centre only
-    const bool mirror = g.centre >= 0 && imap_t == nullptr && g.K == 2 * g.centre + 1;
+    // submanifold maps (centre >= 0, odd kernels) are probed for k <= centre only;
+    // the caller has zeroed the mask and filled imap rows k > centre with -1
+    const bool mirror = probe_mirror(g, imap_t != nullptr);
     const int n_probe = mirror ? g.centre + 1 : g.K;
-    if (mask) SPC_CUDA_TRY(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * (size_t)nq, st));
-    if (mirror && g.K > n_probe)
-        SPC_CUDA_TRY(cudaMemsetAsync(imap + (int64_t)n_probe * nq, 0xFF,
-                                     sizeof(int32_t) * (size_t)(g.K - n_probe) * (size_t)nq, st));
     ProbeTab tab;
     for (int k = 0; k < kMaxTab; ++k) {
         int dz = 0, dy = 0, dx = 0;

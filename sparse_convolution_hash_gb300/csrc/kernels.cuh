@@ -39,7 +39,18 @@ struct ProbeGeom {
     int32_t centre;        // offset index that maps each row to itself (subm), or -1
 };
 
-spc_status hash_clear(HashTable t, cudaStream_t st);
+// Buffers a build starts from: each region is filled with a 32-bit pattern.
+struct FillRegion {
+    uint32_t* p;
+    int64_t n;   // 32-bit words
+    uint32_t v;
+};
+struct FillList {
+    FillRegion r[5];
+};
+spc_status build_init(const FillList& L, int n, cudaStream_t st);
+// True when the probe fills a submanifold map through offset mirrors (k <= centre).
+bool probe_mirror(const ProbeGeom& g, bool with_transpose);
 spc_status hash_insert(const int32_t* coords, int64_t n, int32_t batch, const int32_t shape[3],
                        HashTable t, int32_t* status, cudaStream_t st);
 spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const ProbeGeom& g,
