@@ -35,6 +35,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -84,7 +85,9 @@ class Clocks:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples; the JSON line carries their summary
+        self.path = os.path.join(os.environ.get("SPC_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"spc_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
