@@ -84,8 +84,12 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     t /= tiles_j;
     const int ct = t % tiles_c;
     const int kg = t / tiles_c;
-    const int k0 = kg * kGroup;
-    const int ng = a.K - k0 < kGroup ? a.K - k0 : kGroup;
+    // the K offsets are split into ceil(K / kGroup) groups of near-equal size
+    // (27 -> 7, 7, 7, 6), so every CTA of a row split does the same work
+    const int n_groups = (a.K + kGroup - 1) / kGroup;
+    const int g_base = a.K / n_groups, g_rem = a.K % n_groups;
+    const int k0 = kg * g_base + (kg < g_rem ? kg : g_rem);
+    const int ng = g_base + (kg < g_rem ? 1 : 0);
     const int s_split = blockIdx.y;
     const int64_t o_lo = (int64_t)s_split * a.chunk;
     const int64_t o_hi = o_lo + a.chunk < a.n_out ? o_lo + a.chunk : a.n_out;
@@ -322,14 +326,15 @@ bool wgrad_tc_supported(int32_t K, int32_t cin, int32_t cout, spc_dtype dt)
     return (dt == SPC_F16 || dt == SPC_BF16) && K >= 1 && cin % 64 == 0 && cout % 64 == 0;
 }
 
-// Row splits: enough CTAs to fill a GPU of about 160 SMs once.  A fixed target
-// (not the device's SM count) keeps the summation order, and so the result
-// bits, the same on every device.
+// Row splits: at most one CTA per SM of a 152-SM GB300 (a CTA takes all of its
+// SM's tensor memory, so one more CTA than SMs would double the time).  A fixed
+// target (not the device's SM count) keeps the summation order, and so the
+// result bits, the same on every device.
 int wgrad_tc_splits(int32_t K, int64_t n_out, int32_t cin, int32_t cout)
 {
-    constexpr int64_t kTargetCtas = 160;
+    constexpr int64_t kTargetCtas = 152;
     const int64_t tiles = (int64_t)((K + kGroup - 1) / kGroup) * (cin / 64) * (cout / 64);
-    int64_t s = tiles > 0 ? (kTargetCtas + tiles - 1) / tiles : 1;
+    int64_t s = tiles > 0 ? kTargetCtas / tiles : 1;
     const int64_t max_s = n_out > 0 ? (n_out + kRows - 1) / kRows : 1;
     if (s > max_s) s = max_s;
     return (int)(s < 1 ? 1 : s);
