@@ -62,6 +62,8 @@ DESCRIPTIONS = {
     "shell256_k1_bf16": "SubMConv3d k1 forward (per-voxel GEMM), 256^3 shell, bf16 128->128",
     "shell192x4_train_bf16": "SubMConv3d k3 indice build + forward + dinput + dfilter, "
                              "4 x 192^3 shells, bf16 64->64",
+    "shell256_inverse_bf16": "SparseInverseConv3d of a k3 s2 p1 conv (maps built once), 256^3 "
+                             "shell, bf16 128->128",
 }
 ELEM = {"f32": 4, "f16": 2, "bf16": 2}
 
@@ -217,7 +219,7 @@ class Case:
                     "build", lambda: spc.spc_build_indice_map(
                         self.coords, self.batch, self.shape, ksize=self.ks, subm=True, out=self.m),
                     "build", 16 * n + 4 * K * n + 4 * n + 4 * K,
-                    kernels="k_hash_clear, k_hash_insert, k_map_probe", launches=3))
+                    kernels="k_build_init, k_hash_insert, k_map_probe", launches=3))
             else:
                 self.m = None
                 imap = mask = None
@@ -255,17 +257,36 @@ class Case:
             imap, mask = self.m["imap"], self.m["mask"]
             cells = self.batch * int(np.prod(list(self.out_shape)))
             passes = (max(1, int(np.ceil(np.log2(max(cells, 2))))) + 7) // 8
-            self.phases.append(Phase("outcoords", outcoords, "build", 16 * n + 16 * n_out + 8,
-                                     kernels="k_candidates, k_radix_*, k_unique_*",
-                                     launches=1 + 3 * passes + 3))
-            self.phases.append(Phase(
-                "build", lambda: spc.spc_build_indice_map(
-                    self.coords, self.batch, self.shape, ksize=self.ks, stride=st, pad=pd,
-                    subm=False, out_coords=self.oc, with_transpose=True, out=self.m),
-                "build", 16 * n + 16 * n_out + 4 * K * n_out + 4 * K * n + 4 * n_out + 4 * K,
-                kernels="k_hash_clear, k_hash_insert, k_map_probe<imap_t>", launches=3))
+            if not w.get("inverse"):
+                self.phases.append(Phase("outcoords", outcoords, "build", 16 * n + 16 * n_out + 8,
+                                         kernels="k_candidates, k_radix_*, k_unique_*",
+                                         launches=1 + 3 * passes + 3))
+                self.phases.append(Phase(
+                    "build", lambda: spc.spc_build_indice_map(
+                        self.coords, self.batch, self.shape, ksize=self.ks, stride=st, pad=pd,
+                        subm=False, out_coords=self.oc, with_transpose=True, out=self.m),
+                    "build", 16 * n + 16 * n_out + 4 * K * n_out + 4 * K * n + 4 * n_out + 4 * K,
+                    kernels="k_build_init, k_hash_insert, k_map_probe<imap_t>", launches=3))
         n_out, P = self.n_out, self.pairs
         self.imap, self.mask = imap, mask
+        if w.get("inverse"):
+            # the inverse conv runs on the strided conv's maps: its inputs are
+            # features on the output set, its outputs rows of the input set
+            self.inverse = True
+            self.yin = w["y_for"](n_out).to(dev)
+            self.y = torch.empty((n, cout), dtype=self.x.dtype, device=dev)
+            nbw = int(B.lib().spc_conv_workspace_size(K, n_out, n, cin, cout, B._DTYPES[self.x.dtype]))
+            self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
+            self.train = False
+            self.phases.append(Phase(
+                "inverse", lambda: spc.spc_conv_inverse(self.yin, self.wt, self.bias, self.m["imap_t"],
+                                                        precision=self.prec, out=self.y,
+                                                        status=self.status, ws=self.conv_ws),
+                "conv", s * n_out * cin + s * n * cout + s * K * cin * cout + 4 * P,
+                2.0 * P * cin * cout, kernels=self.fwd_kernel(),
+                launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+            return
+        self.inverse = False
         self.y = torch.empty((n_out, cout), dtype=self.x.dtype, device=dev)
         nbw = int(B.lib().spc_conv_workspace_size(K, n, n_out, cin, cout, B._DTYPES[self.x.dtype]))
         self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
@@ -336,6 +357,13 @@ class Case:
 
     # -- end to end through the C ABI from pinned host memory
     def setup_e2e(self):
+        if self.inverse:
+            # the maps are saved from the strided conv: a step moves features and weights
+            self.h_in = [(self.yin.cpu().pin_memory(), self.yin), (self.w["w"].pin_memory(), self.wt)]
+            self.h_out = [(torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory(), self.y)]
+            self.h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
+            self.d2h = sum(h.numel() * h.element_size() for h, _ in self.h_out)
+            return
         self.h_in = [(self.coords_h.pin_memory(), self.coords), (self.w["x"].pin_memory(), self.x),
                      (self.w["w"].pin_memory(), self.wt)]
         if self.bias is not None:
@@ -427,7 +455,7 @@ def record_traffic(csv_path: str, workload: str, phases):
     fwd, dgr = (conv[0::2], conv[1::2]) if "dgrad" in phases else (conv, [])
     tr = k(r"k_transpose_w")
     if fwd:
-        got["fwd"] = sum(d["bytes"] for d in fwd) / len(fwd) + (
+        got["inverse" if "inverse" in phases else "fwd"] = sum(d["bytes"] for d in fwd) / len(fwd) + (
             sum(d["bytes"] for d in tr) / len(tr) if tr else 0.0)
     if dgr:
         got["dgrad"] = sum(d["bytes"] for d in dgr) / len(dgr)
@@ -589,6 +617,21 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
         oc = oracle.strided_out_coords(c, batch, shape, ks, stride, pad, 1)
         imap, _, cnt = oracle.strided_map(c, oc, batch, shape, ks, stride, pad, 1, False)
     t_map = time.perf_counter() - t0
+    if case_w.get("inverse"):
+        # the inverse conv on the saved maps (not charged): a sample of the
+        # strided output rows scattered back through their pairs
+        n_y = imap.shape[1]
+        y64 = oracle.f64(case_w["y_for"](n_y))
+        per_col = 2.0 * float(cnt.sum()) / max(n_y, 1) * cin * cout
+        cols = int(min(n_y, max(64, budget_s * 1.0e9 / max(per_col, 1.0))))
+        sel = np.linspace(0, n_y - 1, cols).astype(np.int64)
+        sub = np.ascontiguousarray(imap[:, sel])
+        t1 = time.perf_counter()
+        oracle.conv_inverse(y64[sel], w64, b64, sub, n)
+        t = time.perf_counter() - t1
+        flops = 2.0 * float((sub >= 0).sum()) * cin * cout
+        return flops / t / 1e12, (f"fp64 inverse conv of {cols} of {n_y} strided output rows "
+                                  f"(maps built once, not charged), {t:.1f} s, single thread")
     n_out = imap.shape[1]
     per_row = 2.0 * float(cnt.sum()) / max(n_out, 1) * cin * cout  # flops per output row
     # rows so that the forward sample takes about the budget at ~1 GFLOP/s
@@ -672,6 +715,8 @@ def main():
         phases = (["build"] if w["subm"] and w["k"] > 1 else []) + \
                  ([] if w["subm"] else ["outcoords", "build"]) + ["fwd"] + \
                  (["dgrad", "wgrad"] if w.get("train") else [])
+        if w.get("inverse"):
+            phases = ["inverse"]
         record_traffic(args.record_traffic, args.workload, phases)
         return
     args.warmup = max(args.warmup, 3)

@@ -220,10 +220,11 @@ SPC_API spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, i
  *  ws    spc_conv_workspace_size(...) bytes (the tensor-core path keeps the
  *        weights transposed to [K, Cout, Cin] there).
  *  x, w, y must be 16-byte aligned.
- *  Kernels: tcgen05 tensor cores when the channels allow (fp16 / bf16 with
- *  Cin % 64 == 0, or fp32 with SPC_PREC_TF32 and Cin % 32 == 0; Cout % 64 ==
- *  0; K <= 32), a one-row-per-thread kernel for narrow channels (Cin, Cout in
- *  {8, 16, 32}), else a tiled CUDA-core kernel.
+ *  Kernels: a one-row-per-thread kernel when Cin and Cout are both in
+ *  {8, 16, 32} (narrow layers on sparse scenes are latency-bound); else
+ *  tcgen05 tensor cores when the channels allow (fp16 / bf16 with Cin % 64 ==
+ *  0, or 16 / 32 with Cout % 64 == 0, or fp32 with SPC_PREC_TF32 and Cin % 32
+ *  == 0; Cout % 64 == 0 or in {16, 32}; K <= 32); else a tiled CUDA-core kernel.
  */
 SPC_API size_t spc_conv_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
                                int32_t cout, spc_dtype dt);
@@ -233,6 +234,31 @@ SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias,
                                 int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
                                 spc_dtype dt, spc_precision prec, void* y, int32_t* status,
                                 void* ws, size_t ws_bytes, void* stream);
+
+/* spc_conv_inverse -- out[i, :] = bias + sum over pairs imap[k, o] = i of y[o, :] W[k]
+ * (spconv SparseInverseConv3d, "spconv.pytorch Layer APIs Reference" and "Using
+ * SparseInverseConv for Inverse Sparse Operations": the inverse of a strided
+ * conv that shares its indice key; it brings features on the strided conv's
+ * output set back to that conv's input set through the same pairs).  Read
+ * through the strided conv's transposed map, it is a gathered conv like
+ * spc_conv_fwd with the roles of the two coordinate sets exchanged, and runs on
+ * the same kernels.  Its gradients are spc_conv_dgrad with the forward map imap
+ * as SPC_MAP_TRANSPOSED (dy = sum over pairs of W[k] dout[i]) and
+ * spc_conv_wgrad(y, dout, imap_t) (dW[k] = sum over pairs of y[o]^T dout[i]).
+ *
+ *  y      [n_y, cy] of dtype dt: features on the strided conv's output set.
+ *  w      [K, cy, cout] of dtype dt.   bias [cout] or NULL.
+ *  imap_t [K, n_out] int32: the strided conv's transposed map from
+ *         spc_build_indice_map (imap_t[k, i] = o exactly when imap[k, o] = i).
+ *  out    [n_out, cout] of dtype dt out: rows of the strided conv's input set.
+ *  ws     spc_conv_workspace_size(K, n_y, n_out, cy, cout, dt) bytes.
+ *  Errors and alignment as for spc_conv_fwd.
+ */
+SPC_API spc_status spc_conv_inverse(const void* y, const void* w, const void* bias,
+                                    const int32_t* imap_t, int32_t K, int64_t n_y, int64_t n_out,
+                                    int32_t cy, int32_t cout, spc_dtype dt, spc_precision prec,
+                                    void* out, int32_t* status, void* ws, size_t ws_bytes,
+                                    void* stream);
 
 /* spc_conv_dgrad -- dx[i, :] = sum over pairs imap[k, o] = i of W[k] dy[o, :]
  * (the gradient of spc_conv_fwd with respect to x; "dinput" in the HYGON-AI

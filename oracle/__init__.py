@@ -73,6 +73,9 @@ def _load():
             lib.orc_conv_fwd_rows.argtypes = [_F64P, _F64P, ctypes.c_void_p, _I32P, _i64, _i64,
                                               _i64, _i32, _i32, _I64P, _i64, _F64P]
             lib.orc_conv_fwd_rows.restype = None
+            lib.orc_conv_inverse.argtypes = [_F64P, _F64P, ctypes.c_void_p, _I32P, _i64, _i64, _i64,
+                                             _i32, _i32, _F64P]
+            lib.orc_conv_inverse.restype = None
             lib.orc_conv_dgrad.argtypes = [_F64P, _F64P, _I32P, _i64, _i64, _i64, _i32, _i32, _F64P]
             lib.orc_conv_dgrad.restype = None
             lib.orc_conv_dgrad_rows.argtypes = [_F64P, _F64P, _I32P, _i64, _i64, _i64, _i32, _i32,
@@ -193,6 +196,21 @@ def conv_fwd(x, w, bias, imap, rows=None):
     y = np.empty((r.shape[0], cout), dtype=np.float64)
     lib.orc_conv_fwd_rows(x, w, bptr, m, K, n_in, n_out, cin, cout, r, r.shape[0], y)
     return y
+
+
+def conv_inverse(y, w, bias, imap, n_out: int):
+    """Inverse conv of a strided conv with forward map imap [K, N_y]:
+    out[i] = bias + sum over pairs imap[k, o] = i of y[o] W[k], out [n_out, Cout]."""
+    lib = _load()
+    y, w = f64(y), f64(w)
+    b = f64(bias) if bias is not None else None
+    m = np.ascontiguousarray(imap, dtype=np.int32)
+    K, n_y = m.shape
+    cy, cout = w.shape[1], w.shape[2]
+    assert y.shape == (n_y, cy) and w.shape[0] == K
+    out = np.empty((n_out, cout), dtype=np.float64)
+    lib.orc_conv_inverse(y, w, b.ctypes.data if b is not None else None, m, K, n_y, n_out, cy, cout, out)
+    return out
 
 
 def conv_dgrad(dy, w, imap, n_in: int):

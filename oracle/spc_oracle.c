@@ -342,6 +342,37 @@ void orc_conv_dgrad(const double* dy, const double* w, const int32_t* imap, int6
     }
 }
 
+/*
+ * Inverse conv (spconv SparseInverseConv3d, "spconv.pytorch Core Concepts
+ * Definitions" / common usage: the inverse of a strided conv that shares its
+ * indice key restores the strided conv's input coordinate set).  For every pair
+ * (k, o, i) of the strided conv's map imap [K, n_y] (imap[k, o] = i): the
+ * feature y[o] of strided output o goes back to input site i through W[k]:
+ *     out[i, :] = bias + sum over pairs with imap[k, o] = i of y[o, :] W[k],
+ * W [K, cy, cout].  Written as a scatter over the forward map, so it shares no
+ * loop with orc_conv_fwd (which gathers through a map of the output rows).
+ */
+void orc_conv_inverse(const double* y, const double* w, const double* bias, const int32_t* imap,
+                      int64_t K, int64_t n_y, int64_t n_out, int32_t cy, int32_t cout, double* out)
+{
+    for (int64_t i = 0; i < n_out; ++i)
+        for (int32_t j = 0; j < cout; ++j) out[i * cout + j] = bias ? bias[j] : 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double* wk = w + k * cy * cout;
+        for (int64_t o = 0; o < n_y; ++o) {
+            const int32_t i = imap[k * n_y + o];
+            if (i < 0) continue;
+            const double* f = y + o * cy;
+            double* d = out + (int64_t)i * cout;
+            for (int32_t j = 0; j < cout; ++j) {
+                double s = 0.0;
+                for (int32_t c = 0; c < cy; ++c) s += f[c] * wk[(int64_t)c * cout + j];
+                d[j] += s;
+            }
+        }
+    }
+}
+
 /* dinput at the listed input rows, through a transposed map imap_t [K, n_in]. */
 void orc_conv_dgrad_rows(const double* dy, const double* w, const int32_t* imap_t, int64_t K,
                          int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,

@@ -206,6 +206,11 @@ WORKLOADS = {
     "shell192x4_train_bf16": dict(coords=("shell192x4",), batch=4, shape=(192, 192, 192), k=3,
                                   stride=1, pad=1, subm=True, dtype="bf16", cin=64, cout=64,
                                   bias_var=None, seed=5, train=True),
+    # inverse of a k3 s2 p1 conv on the 256^3 shell: features on the strided output set
+    # (cin channels) go back to the shell's voxels (cout channels)
+    "shell256_inverse_bf16": dict(coords=("shell256",), batch=1, shape=(256, 256, 256), k=3,
+                                  stride=2, pad=1, subm=False, dtype="bf16", cin=128, cout=128,
+                                  bias_var=None, seed=9, inverse=True),
 }
 
 _COORD_CACHE: dict = {}
@@ -250,4 +255,7 @@ def workload(name: str) -> dict:
                    if spec["bias_var"] is not None else None)
     if spec["subm"]:
         out["dy"] = normal((n, cout), 1.0, dt, seed, 4)
+    if spec.get("inverse"):
+        # features on the strided output set, whose size the caller finds first
+        out["y_for"] = lambda n_y: normal((n_y, cin), 1.0, dt, seed, 5)
     return out

@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     spc_build_indice_map,
     spc_conv_dgrad,
     spc_conv_fwd,
+    spc_conv_inverse,
     spc_conv_wgrad,
     spc_out_shape,
     spc_strided_out_coords,

@@ -107,6 +107,9 @@ def lib():
             L.spc_conv_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
                                        _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd.restype = _i32
+            L.spc_conv_inverse.argtypes = [_p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32, _i32,
+                                           _p, _p, _p, _sz, _p]
+            L.spc_conv_inverse.restype = _i32
             L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _i32, _i64, _i64, _i32, _i32,
                                          _i32, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_dgrad.restype = _i32
@@ -273,6 +276,30 @@ def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
                               0 if ws is None else ws.numel(), _stream(x.device))
     _check(code, "spc_conv_fwd")
     return y
+
+
+def spc_conv_inverse(y: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                     imap_t: torch.Tensor, precision: int = SPC_PREC_EXACT,
+                     out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                     ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Inverse of a strided conv through its transposed map imap_t [K, N_in]:
+    out[i] = bias + sum over pairs imap_t[k, i] = o of y[o] W[k]; out [N_in, Cout]."""
+    y = _cuda(y, "y")
+    w = _cuda(w, "w").to(y.dtype)
+    b = _cuda(bias, "bias").to(y.dtype) if bias is not None else None
+    m = _cuda(imap_t, "imap_t")
+    K, cy, cout = w.shape
+    n_out = m.shape[1]
+    o = torch.empty((n_out, cout), dtype=y.dtype, device=y.device) if out is None else out
+    dt = _DTYPES[y.dtype]
+    nbytes = int(lib().spc_conv_workspace_size(K, y.shape[0], n_out, cy, cout, dt))
+    if nbytes and (ws is None or ws.numel() < nbytes):
+        ws = _workspace(nbytes, y.device)
+    code = lib().spc_conv_inverse(_ptr(y), _ptr(w), _ptr(b), _ptr(m), K, y.shape[0], n_out, cy,
+                                  cout, dt, precision, _ptr(o), _ptr(status), _ptr(ws),
+                                  0 if ws is None else ws.numel(), _stream(y.device))
+    _check(code, "spc_conv_inverse")
+    return o
 
 
 def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tensor], kind: int,

@@ -287,6 +287,18 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
     return run_gather(p, dt, st);
 }
 
+spc_status spc_conv_inverse(const void* y, const void* w, const void* bias, const int32_t* imap_t,
+                            int32_t K, int64_t n_y, int64_t n_out, int32_t cy, int32_t cout,
+                            spc_dtype dt, spc_precision prec, void* out, int32_t* status, void* ws,
+                            size_t ws_bytes, void* stream)
+{
+    // the inverse conv gathers through the transposed map: rows of the strided
+    // conv's input set are its outputs, rows of its output set its inputs
+    if (n_out > 0 && !imap_t) return SPC_ERR_INVALID_ARG;
+    return spc_conv_fwd(y, w, bias, imap_t, nullptr, K, n_y, n_out, cy, cout, dt, prec, out, status,
+                        ws, ws_bytes, stream);
+}
+
 spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
                           const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
                           int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec, void* dx,

@@ -113,6 +113,15 @@ def test_argument_errors_return_before_any_work(L):
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(258), None, ctypes.c_void_p(256),
                           None, 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0,
                           None) == E
+    # inverse conv: the transposed map is required; bad dtype and misaligned weight rejected
+    assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, 27, 4, 4,
+                              8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0, None) == E
+    assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(256), None,
+                              ctypes.c_void_p(256), 27, 4, 4, 8, 8, 7, 0, ctypes.c_void_p(256),
+                              None, None, 0, None) == E
+    assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(258), None,
+                              ctypes.c_void_p(256), 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256),
+                              None, None, 0, None) == E
     # the tensor-core path needs its workspace (transposed weights)
     assert L.spc_conv_workspace_size(27, 4, 4, 128, 128, binding.SPC_BF16) == 27 * 128 * 128 * 2
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256),

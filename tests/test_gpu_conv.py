@@ -126,6 +126,41 @@ def test_uniform32_strided_bf16():
     assert normwise(to_np(dw), oracle.conv_wgrad(w["x"], dy, imap_ref)) < 2e-2
 
 
+@pytest.mark.parametrize("dtype,cy,cout", [("bf16", 128, 64), ("f16", 64, 64), ("f32", 16, 16),
+                                           ("bf16", 32, 32), ("bf16", 64, 16), ("f16", 24, 40)])
+def test_inverse_conv_strided(dtype, cy, cout):
+    """Inverse of the k3 s2 p1 conv on the 2,000-voxel set: output, and both
+    gradients through the documented spc_conv_dgrad / spc_conv_wgrad calls."""
+    w = scenes.workload("uniform32_strided_bf16")
+    c = w["coords"]
+    d = dev()
+    dc = torch.from_numpy(c).to(d)
+    oc, _ = spc.spc_strided_out_coords(dc, 1, (32, 32, 32), 3, 2, 1, 1)
+    m = spc.spc_build_indice_map(dc, 1, (32, 32, 32), ksize=3, stride=2, pad=1, subm=False,
+                                 out_coords=oc, with_transpose=True)
+    spc.check_status(m["status"])
+    oc_ref = oracle.strided_out_coords(c, 1, (32, 32, 32), 3, 2, 1, 1)
+    imap_ref, imap_t_ref, _ = oracle.strided_map(c, oc_ref, 1, (32, 32, 32), 3, 2, 1, 1)
+    g = np.random.default_rng(cy * 1000 + cout)
+    n_y, n = oc.shape[0], c.shape[0]
+    y = rand_tensor(g, (n_y, cy), dtype)
+    wt = rand_tensor(g, (27, cy, cout), dtype, std=float(np.sqrt(1.0 / (27 * cy))))
+    b = rand_tensor(g, (cout,), dtype, std=0.1)
+    tol = TOL[(dtype, "exact")]
+    out = spc.spc_conv_inverse(y.to(d), wt.to(d), b.to(d), m["imap_t"])
+    assert out.shape == (n, cout)
+    assert normwise(to_np(out), oracle.conv_inverse(y, wt, b, imap_ref, n)) < tol
+    assert torch.equal(out, spc.spc_conv_inverse(y.to(d), wt.to(d), b.to(d), m["imap_t"]))
+    dout = rand_tensor(g, (n, cout), dtype)
+    # dy[o] = sum over pairs imap[k, o] = i of W[k] dout[i]: the forward map read as transposed
+    dy = spc.spc_conv_dgrad(dout.to(d), wt.to(d), m["imap"], spc.SPC_MAP_TRANSPOSED, n_y)
+    wt_t = wt.double().numpy().transpose(0, 2, 1)
+    assert normwise(to_np(dy), oracle.conv_fwd(dout, wt_t, None, imap_ref)) < tol
+    # dW[k] = sum over pairs of y[o]^T dout[i]
+    dw = spc.spc_conv_wgrad(y.to(d), dout.to(d), m["imap_t"], 27)
+    assert normwise(to_np(dw), oracle.conv_wgrad(y, dout, imap_t_ref)) < tol
+
+
 @pytest.mark.parametrize("name", ["lidar_subm_f16", "shell256_subm_bf16", "shell256_k1_bf16"])
 def test_forward_workloads_sampled(name):
     w = scenes.workload(name)

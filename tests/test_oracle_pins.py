@@ -250,6 +250,39 @@ def test_strided_fwd_vs_dense_conv3d(shape, ks, stride, pad, dil, batch):
     assert dense.permute(0, 2, 3, 4, 1)[mask].abs().max().item() == 0.0
 
 
+@pytest.mark.parametrize("shape,ks,stride,pad,dil,batch", [
+    ((8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), 2),
+    ((10, 9, 11), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1), 1),
+    ((9, 7, 8), (2, 3, 3), (2, 1, 3), (0, 1, 2), (1, 1, 1), 1),
+])
+def test_inverse_vs_dense_conv_transpose3d(shape, ks, stride, pad, dil, batch):
+    """The inverse conv of a strided conv (same maps) is the dense transposed
+    convolution of the strided output, read back at the input sites."""
+    g = np.random.default_rng(23)
+    coords = rand_coords(g, 80, batch, shape)
+    cy, cout = 4, 3
+    oc = oracle.strided_out_coords(coords, batch, shape, ks, stride, pad, dil)
+    imap, imap_t, _ = oracle.strided_map(coords, oc, batch, shape, ks, stride, pad, dil,
+                                         with_transpose=True)
+    y = feats(g, oc.shape[0], cy)
+    w = g.standard_normal((int(np.prod(ks)), cy, cout))
+    b = g.standard_normal(cout)
+    out = oracle.conv_inverse(y, w, b, imap, coords.shape[0])
+    oshape = oracle.out_shape(shape, ks, stride, pad, dil)
+    opad = [shape[a] - ((oshape[a] - 1) * stride[a] - 2 * pad[a] + dil[a] * (ks[a] - 1) + 1)
+            for a in range(3)]
+    assert all(0 <= opad[a] < max(stride[a], dil[a]) for a in range(3))
+    wt = torch.as_tensor(w, dtype=torch.float64).reshape(*ks, cy, cout).permute(3, 4, 0, 1, 2)
+    dense = F.conv_transpose3d(dense_grid(oc, y, batch, oshape), wt.contiguous(),
+                               torch.as_tensor(b, dtype=torch.float64), stride=stride,
+                               padding=pad, output_padding=opad, dilation=dil)
+    t = torch.as_tensor(coords, dtype=torch.long)
+    np.testing.assert_allclose(out, dense[t[:, 0], :, t[:, 1], t[:, 2], t[:, 3]].numpy(),
+                               rtol=1e-12, atol=1e-12)
+    # the gather form over the transposed map gives the same rows
+    np.testing.assert_allclose(out, oracle.conv_fwd(y, w, b, imap_t), rtol=1e-12, atol=1e-12)
+
+
 def test_k1_is_gemm():
     g = np.random.default_rng(23)
     coords = rand_coords(g, 200, 2, (9, 9, 9))
