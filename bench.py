@@ -62,6 +62,8 @@ DESCRIPTIONS = {
     "shell256_k1_bf16": "SubMConv3d k1 forward (per-voxel GEMM), 256^3 shell, bf16 128->128",
     "shell192x4_train_bf16": "SubMConv3d k3 indice build + forward + dinput + dfilter, "
                              "4 x 192^3 shells, bf16 64->64",
+    "shell192x4_resblock_bf16": "SubMConv3d k3 indice build + forward with fused residual add + "
+                                "ReLU (relu(conv(x) + x)), 4 x 192^3 shells, bf16 64->64",
     "shell256_inverse_bf16": "SparseInverseConv3d of a k3 s2 p1 conv (maps built once), 256^3 "
                              "shell, bf16 128->128",
 }
@@ -292,12 +294,23 @@ class Case:
         self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
         flops = 2.0 * P * cin * cout
         bias_b = s * cout if self.bias is not None else 0
-        self.phases.append(Phase(
-            "fwd", lambda: spc.spc_conv_fwd(self.x, self.wt, self.bias, self.imap, self.mask,
-                                            n_out=n_out, precision=self.prec, out=self.y,
-                                            status=self.status, ws=self.conv_ws),
-            "conv", s * n * cin + s * n_out * cout + s * K * cin * cout + 4 * P + bias_b, flops,
-            kernels=self.fwd_kernel(), launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+        if w.get("resblock"):
+            # residual block tail: the identity is the block input itself
+            self.phases.append(Phase(
+                "fwd", lambda: spc.spc_conv_fwd_fused(
+                    self.x, self.wt, self.bias, self.imap, self.mask, residual=self.x,
+                    add_scale=1.0, act=B.SPC_ACT_RELU, n_out=n_out, precision=self.prec,
+                    out=self.y, status=self.status, ws=self.conv_ws),
+                "conv", s * n * cin + 2 * s * n_out * cout + s * K * cin * cout + 4 * P + bias_b,
+                flops, kernels=self.fwd_kernel() + ", fused residual + ReLU epilogue",
+                launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+        else:
+            self.phases.append(Phase(
+                "fwd", lambda: spc.spc_conv_fwd(self.x, self.wt, self.bias, self.imap, self.mask,
+                                                n_out=n_out, precision=self.prec, out=self.y,
+                                                status=self.status, ws=self.conv_ws),
+                "conv", s * n * cin + s * n_out * cout + s * K * cin * cout + 4 * P + bias_b, flops,
+                kernels=self.fwd_kernel(), launches=2 if "tcgen05" in self.fwd_kernel() else 1))
         self.train = bool(w.get("train"))
         if self.train:
             self.dy = w["dy"].to(dev)

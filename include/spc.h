@@ -78,6 +78,9 @@ typedef enum { SPC_F32 = 0, SPC_F16 = 1, SPC_BF16 = 2 } spc_dtype;
  * multiply (accumulation stays fp32); ignored for fp16/bf16. */
 typedef enum { SPC_PREC_EXACT = 0, SPC_PREC_TF32 = 1 } spc_precision;
 
+/* Activation of the fused forward epilogue (spc_conv_fwd_fused). */
+typedef enum { SPC_ACT_NONE = 0, SPC_ACT_RELU = 1 } spc_activation;
+
 /* How spc_conv_dgrad reads its map argument. */
 typedef enum {
     /* map is the transposed map imap_t [K, n_in]: imap_t[k, i] = o for every
@@ -234,6 +237,30 @@ SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias,
                                 int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
                                 spc_dtype dt, spc_precision prec, void* y, int32_t* status,
                                 void* ws, size_t ws_bytes, void* stream);
+
+/* spc_conv_fwd_fused -- y[o, :] = act(bias + sum_k sum_{i = imap[k, o] != -1} x[i, :] W[k]
+ *                                     + add_scale * residual[o, :])
+ * (spconv docs, "Call Spconv Implicit GEMM with Calculated Scales and Bias":
+ * the implicit GEMM takes a bias, an activation and an added output with its
+ * scale, "for fused conv-add-relu layer"; "Fusible Spconv Residual Block
+ * Example for Quantization": out = relu(conv_bn(x) + identity)).  The residual
+ * add and the activation run in the forward's epilogue on the fp32
+ * accumulators, before the single rounding to dt, so the output is written in
+ * one pass and the residual read once.
+ *
+ *  residual   [n_out, cout] of dtype dt, 16-byte aligned, or NULL (no add);
+ *             it must not be y itself.
+ *  add_scale  factor of the residual (1.0 for a plain residual add).
+ *  act        SPC_ACT_NONE or SPC_ACT_RELU.
+ *  All other arguments, the kernels and the errors as for spc_conv_fwd, which is
+ *  this call with residual NULL and SPC_ACT_NONE.
+ */
+SPC_API spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias,
+                                      const int32_t* imap, const uint32_t* mask, int32_t K,
+                                      int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
+                                      spc_dtype dt, spc_precision prec, const void* residual,
+                                      float add_scale, spc_activation act, void* y,
+                                      int32_t* status, void* ws, size_t ws_bytes, void* stream);
 
 /* spc_conv_inverse -- out[i, :] = bias + sum over pairs imap[k, o] = i of y[o, :] W[k]
  * (spconv SparseInverseConv3d, "spconv.pytorch Layer APIs Reference" and "Using

@@ -198,6 +198,15 @@ def conv_fwd(x, w, bias, imap, rows=None):
     return y
 
 
+def conv_fwd_fused(x, w, bias, imap, residual=None, add_scale=1.0, relu=False):
+    """Forward with the fused epilogue, as defined: act(conv + bias + add_scale residual),
+    act = max(., 0) when relu; all in float64."""
+    y = conv_fwd(x, w, bias, imap)
+    if residual is not None:
+        y = y + float(add_scale) * f64(residual)
+    return np.maximum(y, 0.0) if relu else y
+
+
 def conv_inverse(y, w, bias, imap, n_out: int):
     """Inverse conv of a strided conv with forward map imap [K, N_y]:
     out[i] = bias + sum over pairs imap[k, o] = i of y[o] W[k], out [n_out, Cout]."""

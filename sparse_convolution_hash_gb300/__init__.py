@@ -18,6 +18,9 @@ from .binding import (  # noqa: F401
     spc_build_indice_map,
     spc_conv_dgrad,
     spc_conv_fwd,
+    spc_conv_fwd_fused,
+    SPC_ACT_NONE,
+    SPC_ACT_RELU,
     spc_conv_inverse,
     spc_conv_wgrad,
     spc_out_shape,

@@ -107,6 +107,9 @@ def lib():
             L.spc_conv_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
                                        _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd.restype = _i32
+            L.spc_conv_fwd_fused.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
+                                             _i32, _p, ctypes.c_float, _i32, _p, _p, _p, _sz, _p]
+            L.spc_conv_fwd_fused.restype = _i32
             L.spc_conv_inverse.argtypes = [_p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32, _i32,
                                            _p, _p, _p, _sz, _p]
             L.spc_conv_inverse.restype = _i32
@@ -275,6 +278,40 @@ def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
                               n_out, cin, cout, dt, precision, _ptr(y), _ptr(status), _ptr(ws),
                               0 if ws is None else ws.numel(), _stream(x.device))
     _check(code, "spc_conv_fwd")
+    return y
+
+
+SPC_ACT_NONE, SPC_ACT_RELU = 0, 1
+
+
+def spc_conv_fwd_fused(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                       imap: Optional[torch.Tensor], mask: Optional[torch.Tensor] = None,
+                       residual: Optional[torch.Tensor] = None, add_scale: float = 1.0,
+                       act: int = SPC_ACT_NONE, n_out: Optional[int] = None,
+                       precision: int = SPC_PREC_EXACT, out: Optional[torch.Tensor] = None,
+                       status: Optional[torch.Tensor] = None,
+                       ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y[o] = act(bias + sum over pairs of x[imap[k, o]] W[k] + add_scale residual[o])."""
+    x = _cuda(x, "x")
+    w = _cuda(w, "w").to(x.dtype)
+    b = _cuda(bias, "bias").to(x.dtype) if bias is not None else None
+    res = _cuda(residual, "residual").to(x.dtype) if residual is not None else None
+    K, cin, cout = w.shape
+    if imap is not None:
+        imap = _cuda(imap, "imap")
+        n_out = imap.shape[1]
+    elif n_out is None:
+        n_out = x.shape[0]
+    y = torch.empty((n_out, cout), dtype=x.dtype, device=x.device) if out is None else out
+    dt = _DTYPES[x.dtype]
+    nbytes = int(lib().spc_conv_workspace_size(K, x.shape[0], n_out, cin, cout, dt))
+    if nbytes and (ws is None or ws.numel() < nbytes):
+        ws = _workspace(nbytes, x.device)
+    code = lib().spc_conv_fwd_fused(_ptr(x), _ptr(w), _ptr(b), _ptr(imap), _ptr(mask), K,
+                                    x.shape[0], n_out, cin, cout, dt, precision, _ptr(res),
+                                    float(add_scale), int(act), _ptr(y), _ptr(status), _ptr(ws),
+                                    0 if ws is None else ws.numel(), _stream(x.device))
+    _check(code, "spc_conv_fwd_fused")
     return y
 
 

@@ -232,13 +232,16 @@ spc_status run_gather(const GatherGemm& p, spc_dtype dt, cudaStream_t st)
 
 }  // namespace
 
-spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
-                        const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
-                        int32_t cout, spc_dtype dt, spc_precision prec, void* y, int32_t* status,
-                        void* ws, size_t ws_bytes, void* stream)
+spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias, const int32_t* imap,
+                              const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
+                              int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec,
+                              const void* residual, float add_scale, spc_activation act, void* y,
+                              int32_t* status, void* ws, size_t ws_bytes, void* stream)
 {
     spc_status s = check_conv(x, w, y, K, n_in, n_out, cin, cout, dt);
     if (s != SPC_OK) return s;
+    if (act != SPC_ACT_NONE && act != SPC_ACT_RELU) return SPC_ERR_INVALID_ARG;
+    if (residual && (!aligned16(residual) || residual == y)) return SPC_ERR_INVALID_ARG;
     if (prec != SPC_PREC_EXACT && prec != SPC_PREC_TF32) return SPC_ERR_INVALID_ARG;
     if (!imap && n_out > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
     if (mask && K > 32) return SPC_ERR_INVALID_ARG;
@@ -256,6 +259,9 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
     p.cout = cout;
     p.mirror = 0;
     p.transpose_w = 0;
+    p.residual = residual;
+    p.add_scale = add_scale;
+    p.act = (int32_t)act;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // channel widths of 8 / 16 / 32 on both sides: the latency-oriented CUDA-core
     // kernel (a row has few neighbours on sparse scenes; a tensor-core tile
@@ -281,10 +287,22 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
         a.cred = cin;
         a.n_total = cout;
         a.mirror = 0;
+        a.residual = residual;
+        a.add_scale = add_scale;
+        a.act = (int32_t)act;
         s = conv_gather_tc(a, dt, st);
         if (s != SPC_ERR_UNSUPPORTED) return s;
     }
     return run_gather(p, dt, st);
+}
+
+spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
+                        const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
+                        int32_t cout, spc_dtype dt, spc_precision prec, void* y, int32_t* status,
+                        void* ws, size_t ws_bytes, void* stream)
+{
+    return spc_conv_fwd_fused(x, w, bias, imap, mask, K, n_in, n_out, cin, cout, dt, prec, nullptr,
+                              0.f, SPC_ACT_NONE, y, status, ws, ws_bytes, stream);
 }
 
 spc_status spc_conv_inverse(const void* y, const void* w, const void* bias, const int32_t* imap_t,
@@ -327,6 +345,9 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     p.cout = cin;
     p.mirror = (kind == SPC_MAP_SUBM_MIRROR) ? 1 : 0;
     p.transpose_w = 1;
+    p.residual = nullptr;
+    p.add_scale = 0.f;
+    p.act = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool narrow = conv_narrow_supported(cout, cin, K, dt);
     if (n_in > 0 && !narrow && conv_tc_supported(cout, cin, K, dt, prec) && aligned16(dy) && aligned16(dx)) {
@@ -345,6 +366,9 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
         a.cred = cout;
         a.n_total = cin;
         a.mirror = p.mirror;
+        a.residual = nullptr;
+        a.add_scale = 0.f;
+        a.act = 0;
         const spc_status s2 = conv_gather_tc(a, dt, st);
         if (s2 != SPC_ERR_UNSUPPORTED) return s2;
     }

@@ -182,6 +182,17 @@ __global__ void __launch_bounds__(kThreads, (COUT <= 16 ? 4 : 2)) k_conv_narrow(
                 fma_row<T, CRED, COUT>(acc, xr, s_w + (size_t)k * kStr);
             }
         }
+        if (p.residual) {  // fused residual add, before the activation
+            RowVec<T, COUT> rv;
+            load_row(rv, static_cast<const T*>(p.residual), (int32_t)r);
+            const T* re = reinterpret_cast<const T*>(rv.w);
+#pragma unroll
+            for (int j = 0; j < COUT; ++j) acc[j] = fmaf(p.add_scale, elem<T>::to_f32(re[j]), acc[j]);
+        }
+        if (p.act) {
+#pragma unroll
+            for (int j = 0; j < COUT; ++j) acc[j] = fmaxf(acc[j], 0.f);
+        }
         RowVec<T, COUT> ov;
         T* oe = reinterpret_cast<T*>(ov.w);
 #pragma unroll

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_gemm_simt(GatherGemm p)
 
     T* __restrict__ out = static_cast<T*>(p.out);
     const T* __restrict__ bias = static_cast<const T*>(p.bias);
+    const T* __restrict__ res = static_cast<const T*>(p.residual);
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
         const int64_t r = row0 + tr * 4 + x;
@@ -106,6 +107,8 @@ __global__ void __launch_bounds__(kThreads) k_gather_gemm_simt(GatherGemm p)
             if (j >= p.cout) continue;
             float v = acc[x][y];
             if (bias) v += elem<T>::to_f32(bias[j]);
+            if (res) v = fmaf(p.add_scale, elem<T>::to_f32(res[r * p.cout + j]), v);
+            if (p.act) v = fmaxf(v, 0.f);
             out[r * p.cout + j] = elem<T>::from_f32(v);
         }
     }

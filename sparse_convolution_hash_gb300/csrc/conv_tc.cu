@@ -301,11 +301,21 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
                 }
                 if (evalid) {
                     T* dst = out + erow * a.n_total + n0 + c;
+                    constexpr int kVec = (int)(kCols * sizeof(T) / 16);  // 16-byte words per chunk
+                    alignas(16) T rsd[kCols];
+                    if (a.residual) {
+                        const uint4* r4 = reinterpret_cast<const uint4*>(
+                            static_cast<const T*>(a.residual) + erow * a.n_total + n0 + c);
+#pragma unroll
+                        for (int q = 0; q < kVec; ++q) reinterpret_cast<uint4*>(rsd)[q] = __ldcs(r4 + q);
+                    }
                     alignas(16) T o[kCols];
 #pragma unroll
                     for (int j = 0; j < kCols; ++j) {
                         float f = __uint_as_float(v[j]);
                         if (bias) f += elem<T>::to_f32(bias[n0 + c + j]);
+                        if (a.residual) f = fmaf(a.add_scale, elem<T>::to_f32(rsd[j]), f);
+                        if (a.act) f = fmaxf(f, 0.f);
                         o[j] = elem<T>::from_f32(f);
                     }
                     const uint4* o4 = reinterpret_cast<const uint4*>(o);

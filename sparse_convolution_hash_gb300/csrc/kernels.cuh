@@ -86,6 +86,10 @@ struct GatherGemm {
     int32_t cout;
     int32_t mirror;
     int32_t transpose_w;
+    // fused epilogue: out = act(acc + bias + add_scale * residual), act 1 = ReLU
+    const void* residual;   // [rows, cout] or NULL
+    float add_scale;
+    int32_t act;
 };
 spc_status conv_gather_simt(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
 
@@ -105,6 +109,9 @@ struct TcArgs {
     int32_t* status;
     int64_t rows, in_rows;
     int32_t K, cred, n_total, mirror;
+    const void* residual;   // fused epilogue, as in GatherGemm
+    float add_scale;
+    int32_t act;
 };
 bool conv_tc_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt, spc_precision prec);
 size_t conv_tc_weight_bytes(int32_t K, int32_t cin, int32_t cout, spc_dtype dt);

@@ -113,6 +113,16 @@ def test_argument_errors_return_before_any_work(L):
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(258), None, ctypes.c_void_p(256),
                           None, 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0,
                           None) == E
+    # fused forward: unknown activation, misaligned residual, residual aliasing the output
+    fz = L.spc_conv_fwd_fused
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
+              4, 8, 8, 0, 0, None, 1.0, 2, ctypes.c_void_p(512), None, None, 0, None) == E
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
+              4, 8, 8, 0, 0, ctypes.c_void_p(260), 1.0, 1, ctypes.c_void_p(512), None, None, 0,
+              None) == E
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
+              4, 8, 8, 0, 0, ctypes.c_void_p(512), 1.0, 1, ctypes.c_void_p(512), None, None, 0,
+              None) == E
     # inverse conv: the transposed map is required; bad dtype and misaligned weight rejected
     assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, 27, 4, 4,
                               8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0, None) == E

@@ -126,6 +126,32 @@ def test_uniform32_strided_bf16():
     assert normwise(to_np(dw), oracle.conv_wgrad(w["x"], dy, imap_ref)) < 2e-2
 
 
+@pytest.mark.parametrize("n,cin,cout,dtype,prec", [(777, 16, 16, "f16", "exact"),
+                                                  (1000, 128, 128, "bf16", "exact"),
+                                                  (3000, 64, 64, "bf16", "exact"),
+                                                  (600, 16, 64, "f16", "exact"),
+                                                  (1500, 24, 40, "f32", "exact"),
+                                                  (800, 64, 128, "f32", "tf32")])
+@pytest.mark.parametrize("res_scale,relu", [(1.0, True), (None, True), (0.5, False)])
+def test_fused_epilogue(n, cin, cout, dtype, prec, res_scale, relu):
+    """Residual add and ReLU in the forward's epilogue, on every forward kernel."""
+    g = np.random.default_rng(n + cin)
+    batch, shape = 2, (12, 11, 13)
+    coords = rand_coords(g, n, batch, shape)
+    x, w, b, _, m, imap_ref = subm_case(coords, batch, shape, cin, cout, dtype, seed=n)
+    res = rand_tensor(g, (n, cout), dtype) if res_scale is not None else None
+    d = dev()
+    p = spc.SPC_PREC_TF32 if prec == "tf32" else spc.SPC_PREC_EXACT
+    y = spc.spc_conv_fwd_fused(x.to(d), w.to(d), b.to(d), m["imap"], m["mask"],
+                               residual=res.to(d) if res is not None else None,
+                               add_scale=res_scale if res_scale is not None else 1.0,
+                               act=spc.SPC_ACT_RELU if relu else spc.SPC_ACT_NONE, precision=p)
+    ref = oracle.conv_fwd_fused(x, w, b, imap_ref, res, res_scale or 1.0, relu)
+    assert normwise(to_np(y), ref) < TOL[(dtype, prec)]
+    if relu:
+        assert (to_np(y) >= 0).all()
+
+
 @pytest.mark.parametrize("dtype,cy,cout", [("bf16", 128, 64), ("f16", 64, 64), ("f32", 16, 16),
                                            ("bf16", 32, 32), ("bf16", 64, 16), ("f16", 24, 40)])
 def test_inverse_conv_strided(dtype, cy, cout):

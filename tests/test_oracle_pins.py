@@ -283,6 +283,30 @@ def test_inverse_vs_dense_conv_transpose3d(shape, ks, stride, pad, dil, batch):
     np.testing.assert_allclose(out, oracle.conv_fwd(y, w, b, imap_t), rtol=1e-12, atol=1e-12)
 
 
+def test_fused_epilogue_vs_dense_conv3d_relu():
+    """conv + bias + s * residual, then ReLU: torch's dense conv3d and relu on a
+    zero-filled grid, read at the occupied cells."""
+    g = np.random.default_rng(31)
+    shape, batch, ks = (7, 6, 8), 2, (3, 3, 3)
+    coords = rand_coords(g, 90, batch, shape)
+    cin, cout = 4, 5
+    x = feats(g, 90, cin)
+    w = g.standard_normal((27, cin, cout))
+    b = g.standard_normal(cout)
+    res = g.standard_normal((90, cout))
+    imap, _ = oracle.subm_map(coords, batch, shape, 3)
+    dense = F.conv3d(dense_grid(coords, x, batch, shape), dense_weight(w, ks),
+                     torch.as_tensor(b, dtype=torch.float64), padding=1)
+    t = torch.as_tensor(coords, dtype=torch.long)
+    at = dense[t[:, 0], :, t[:, 1], t[:, 2], t[:, 3]]
+    ref = torch.relu(at + 0.75 * torch.as_tensor(res)).numpy()
+    got = oracle.conv_fwd_fused(x, w, b, imap, res, 0.75, relu=True)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    assert (got == 0).any() and (got > 0).any()  # the activation acts
+    np.testing.assert_allclose(oracle.conv_fwd_fused(x, w, b, imap), at.numpy(), rtol=1e-12,
+                               atol=1e-12)
+
+
 def test_k1_is_gemm():
     g = np.random.default_rng(23)
     coords = rand_coords(g, 200, 2, (9, 9, 9))
