@@ -64,6 +64,8 @@ DESCRIPTIONS = {
                              "4 x 192^3 shells, bf16 64->64",
     "shell192x4_resblock_bf16": "SubMConv3d k3 indice build + forward with fused residual add + "
                                 "ReLU (relu(conv(x) + x)), 4 x 192^3 shells, bf16 64->64",
+    "shell256_maxpool_bf16": "SparseMaxPool3d k2 s2 forward (with argmax) + input gradient "
+                             "(maps built once), 256^3 shell, bf16 128 channels",
     "shell256_inverse_bf16": "SparseInverseConv3d of a k3 s2 p1 conv (maps built once), 256^3 "
                              "shell, bf16 128->128",
 }
@@ -271,6 +273,28 @@ class Case:
                     kernels="k_build_init, k_hash_insert, k_map_probe<imap_t>", launches=3))
         n_out, P = self.n_out, self.pairs
         self.imap, self.mask = imap, mask
+        if w.get("maxpool"):
+            # pooling on the strided map of its window: forward with argmax, then
+            # the input gradient through the transposed map
+            self.inverse = False
+            self.maxpool = True
+            self.train = False
+            self.y = torch.empty((n_out, cin), dtype=self.x.dtype, device=dev)
+            self.arg = torch.empty((n_out, cin), dtype=torch.uint8, device=dev)
+            self.dyp = scenes.normal((n_out, cin), 1.0, self.dtype, w["seed"], 6).to(dev)
+            self.dxp = torch.empty((n, cin), dtype=self.x.dtype, device=dev)
+            self.phases.append(Phase(
+                "pool", lambda: spc.spc_maxpool_fwd(self.x, self.imap, self.mask, out=self.y,
+                                                    arg=self.arg),
+                "conv", s * n * cin + s * n_out * cin + n_out * cin + 4 * P + 4 * n_out,
+                float(P * cin), kernels="k_maxpool_fwd"))
+            self.phases.append(Phase(
+                "pool_dgrad", lambda: spc.spc_maxpool_dgrad(self.dyp, self.m["imap_t"], self.arg,
+                                                            out=self.dxp),
+                "conv", s * n_out * cin + n_out * cin + 4 * K * n + s * n * cin, float(P * cin),
+                kernels="k_maxpool_dgrad"))
+            return
+        self.maxpool = False
         if w.get("inverse"):
             # the inverse conv runs on the strided conv's maps: its inputs are
             # features on the output set, its outputs rows of the input set
@@ -370,6 +394,12 @@ class Case:
 
     # -- end to end through the C ABI from pinned host memory
     def setup_e2e(self):
+        if self.maxpool:
+            self.h_in = [(self.w["x"].pin_memory(), self.x), (self.dyp.cpu().pin_memory(), self.dyp)]
+            self.h_out = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in (self.y, self.dxp)]
+            self.h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
+            self.d2h = sum(h.numel() * h.element_size() for h, _ in self.h_out)
+            return
         if self.inverse:
             # the maps are saved from the strided conv: a step moves features and weights
             self.h_in = [(self.yin.cpu().pin_memory(), self.yin), (self.w["w"].pin_memory(), self.wt)]
@@ -474,6 +504,9 @@ def record_traffic(csv_path: str, workload: str, phases):
         got["dgrad"] = sum(d["bytes"] for d in dgr) / len(dgr)
     if "wgrad" in phases:
         got["wgrad"] = per_call(k(r"k_wgrad"), r"k_wgrad_(tc|partial)")
+    if "pool" in phases:
+        got["pool"] = per_call(k(r"k_maxpool_fwd"), r"k_maxpool_fwd")
+        got["pool_dgrad"] = per_call(k(r"k_maxpool_dgrad"), r"k_maxpool_dgrad")
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -630,6 +663,14 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
         oc = oracle.strided_out_coords(c, batch, shape, ks, stride, pad, 1)
         imap, _, cnt = oracle.strided_map(c, oc, batch, shape, ks, stride, pad, 1, False)
     t_map = time.perf_counter() - t0
+    if case_w.get("maxpool"):
+        # max pool forward on the saved map (not charged), all rows
+        t1 = time.perf_counter()
+        oracle.maxpool_fwd(x64, imap)
+        t = time.perf_counter() - t1
+        return float(cnt.sum()) * cin / t / 1e12, (f"fp64 max pool of all {imap.shape[1]} output "
+                                                   f"rows (map built once, not charged), {t:.1f} s, "
+                                                   f"single thread")
     if case_w.get("inverse"):
         # the inverse conv on the saved maps (not charged): a sample of the
         # strided output rows scattered back through their pairs
@@ -730,6 +771,8 @@ def main():
                  (["dgrad", "wgrad"] if w.get("train") else [])
         if w.get("inverse"):
             phases = ["inverse"]
+        if w.get("maxpool"):
+            phases = ["pool", "pool_dgrad"]
         record_traffic(args.record_traffic, args.workload, phases)
         return
     args.warmup = max(args.warmup, 3)

@@ -287,6 +287,40 @@ SPC_API spc_status spc_conv_inverse(const void* y, const void* w, const void* bi
                                     void* out, int32_t* status, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* ------------------------------------------------------------------ pooling
+ * spc_maxpool_fwd -- y[o, c] = max over the pairs imap[k, o] = i of x[i, c]
+ * (spconv SparseMaxPool3d, "spconv.pytorch Layer APIs Reference": downsampling
+ * whose dense version is nn.MaxPool3d).  The maximum is over the occupied
+ * inputs of o's window only, i.e. the dense max pool of a grid holding
+ * -infinity at empty cells; on the output set of a strided map every row has
+ * at least one pair.  imap is the strided map of the pool's kernel, stride and
+ * padding from spc_build_indice_map (subm = 0).
+ *
+ *  x     [n_in, c] of dtype dt.   y [n_out, c] of dtype dt out (exact: a max).
+ *  imap  [K, n_out] int32.        mask [n_out] uint32 or NULL (lets rows skip
+ *        offsets without a pair).
+ *  arg   [n_out, c] uint8 out or NULL: the first offset k (in offset order)
+ *        reaching the maximum, 255 for a row without pairs (whose y is 0);
+ *        needed by spc_maxpool_dgrad.
+ *  K <= 254 (K <= 32 with a mask); x, y 16-byte aligned for vector access.
+ */
+SPC_API spc_status spc_maxpool_fwd(const void* x, const int32_t* imap, const uint32_t* mask,
+                                   int32_t K, int64_t n_in, int64_t n_out, int32_t c,
+                                   spc_dtype dt, void* y, uint8_t* arg, void* stream);
+
+/* spc_maxpool_dgrad -- dx[i, c] = sum over the pairs imap[k, o] = i with
+ * arg[o, c] == k of dy[o, c] (the gradient of spc_maxpool_fwd: each output
+ * channel passes its gradient to the input it took).  Read through the
+ * transposed map, one write per row of dx, no atomics.
+ *
+ *  dy     [n_out, c] of dtype dt.   imap_t [K, n_in] int32 (the pool map's
+ *         transpose, spc_build_indice_map with imap_t).   arg from
+ *         spc_maxpool_fwd.   dx [n_in, c] of dtype dt out.
+ */
+SPC_API spc_status spc_maxpool_dgrad(const void* dy, const int32_t* imap_t, const uint8_t* arg,
+                                     int32_t K, int64_t n_in, int64_t n_out, int32_t c,
+                                     spc_dtype dt, void* dx, void* stream);
+
 /* spc_conv_dgrad -- dx[i, :] = sum over pairs imap[k, o] = i of W[k] dy[o, :]
  * (the gradient of spc_conv_fwd with respect to x; "dinput" in the HYGON-AI
  * spconv-das README, Testing and Accuracy).  Computed input-stationary through

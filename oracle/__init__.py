@@ -73,6 +73,12 @@ def _load():
             lib.orc_conv_fwd_rows.argtypes = [_F64P, _F64P, ctypes.c_void_p, _I32P, _i64, _i64,
                                               _i64, _i32, _i32, _I64P, _i64, _F64P]
             lib.orc_conv_fwd_rows.restype = None
+            lib.orc_maxpool_fwd.argtypes = [_F64P, _I32P, _i64, _i64, _i64, _i32, _F64P,
+                                            ctypes.c_void_p]
+            lib.orc_maxpool_fwd.restype = None
+            lib.orc_maxpool_dgrad.argtypes = [_F64P, _I32P, ctypes.c_void_p, _i64, _i64, _i64, _i32,
+                                              _F64P]
+            lib.orc_maxpool_dgrad.restype = None
             lib.orc_conv_inverse.argtypes = [_F64P, _F64P, ctypes.c_void_p, _I32P, _i64, _i64, _i64,
                                              _i32, _i32, _F64P]
             lib.orc_conv_inverse.restype = None
@@ -205,6 +211,32 @@ def conv_fwd_fused(x, w, bias, imap, residual=None, add_scale=1.0, relu=False):
     if residual is not None:
         y = y + float(add_scale) * f64(residual)
     return np.maximum(y, 0.0) if relu else y
+
+
+def maxpool_fwd(x, imap):
+    """Max over each output row's pairs (occupied inputs only); returns (y, arg) with
+    arg[o, c] the first offset reaching the max (255 when the row has no pair)."""
+    lib = _load()
+    x = f64(x)
+    m = np.ascontiguousarray(imap, dtype=np.int32)
+    K, n_out = m.shape
+    n_in, c = x.shape
+    y = np.empty((n_out, c), dtype=np.float64)
+    arg = np.empty((n_out, c), dtype=np.uint8)
+    lib.orc_maxpool_fwd(x, m, K, n_in, n_out, c, y, arg.ctypes.data)
+    return y, arg
+
+
+def maxpool_dgrad(dy, imap, arg, n_in: int):
+    lib = _load()
+    dy = f64(dy)
+    m = np.ascontiguousarray(imap, dtype=np.int32)
+    K, n_out = m.shape
+    c = dy.shape[1]
+    a = np.ascontiguousarray(arg, dtype=np.uint8)
+    dx = np.empty((n_in, c), dtype=np.float64)
+    lib.orc_maxpool_dgrad(dy, m, a.ctypes.data, K, n_in, n_out, c, dx)
+    return dx
 
 
 def conv_inverse(y, w, bias, imap, n_out: int):

@@ -373,6 +373,52 @@ void orc_conv_inverse(const double* y, const double* w, const double* bias, cons
     }
 }
 
+/*
+ * Sparse max pooling (spconv SparseMaxPool3d, "spconv.pytorch Layer APIs
+ * Reference": a downsampling layer whose dense version is nn.MaxPool3d), on the
+ * strided map of its kernel / stride / padding: for each output row o and
+ * channel c, the largest x[i, c] over the pairs imap[k, o] = i, taken over the
+ * occupied inputs only (the dense max pool of a grid that holds -infinity at
+ * empty cells).  arg[o, c] is the first k (in offset order) that reaches the
+ * maximum, 255 for a row without pairs (whose output is 0).
+ */
+void orc_maxpool_fwd(const double* x, const int32_t* imap, int64_t K, int64_t n_in, int64_t n_out,
+                     int32_t c, double* y, uint8_t* arg)
+{
+    (void)n_in;
+    for (int64_t o = 0; o < n_out; ++o)
+        for (int32_t j = 0; j < c; ++j) {
+            double best = 0.0;
+            int found = -1;
+            for (int64_t k = 0; k < K; ++k) {
+                const int32_t i = imap[k * n_out + o];
+                if (i < 0) continue;
+                const double v = x[(int64_t)i * c + j];
+                if (found < 0 || v > best) {
+                    best = v;
+                    found = (int)k;
+                }
+            }
+            y[o * c + j] = found < 0 ? 0.0 : best;
+            arg[o * c + j] = (uint8_t)(found < 0 ? 255 : found);
+        }
+}
+
+/* Its input gradient: dy[o, c] goes to the input row of the pair at arg[o, c]. */
+void orc_maxpool_dgrad(const double* dy, const int32_t* imap, const uint8_t* arg, int64_t K,
+                       int64_t n_in, int64_t n_out, int32_t c, double* dx)
+{
+    (void)K;
+    for (int64_t j = 0; j < n_in * c; ++j) dx[j] = 0.0;
+    for (int64_t o = 0; o < n_out; ++o)
+        for (int32_t j = 0; j < c; ++j) {
+            const int k = arg[o * c + j];
+            if (k == 255) continue;
+            const int32_t i = imap[(int64_t)k * n_out + o];
+            dx[(int64_t)i * c + j] += dy[o * c + j];
+        }
+}
+
 /* dinput at the listed input rows, through a transposed map imap_t [K, n_in]. */
 void orc_conv_dgrad_rows(const double* dy, const double* w, const int32_t* imap_t, int64_t K,
                          int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,

@@ -210,6 +210,10 @@ WORKLOADS = {
     "shell192x4_resblock_bf16": dict(coords=("shell192x4",), batch=4, shape=(192, 192, 192), k=3,
                                      stride=1, pad=1, subm=True, dtype="bf16", cin=64, cout=64,
                                      bias_var=None, seed=10, resblock=True),
+    # max pool k2 s2 (forward + gradient) on the 256^3 shell, 128 channels
+    "shell256_maxpool_bf16": dict(coords=("shell256",), batch=1, shape=(256, 256, 256), k=2,
+                                  stride=2, pad=0, subm=False, dtype="bf16", cin=128, cout=128,
+                                  bias_var=None, seed=11, maxpool=True),
     # inverse of a k3 s2 p1 conv on the 256^3 shell: features on the strided output set
     # (cin channels) go back to the shell's voxels (cout channels)
     "shell256_inverse_bf16": dict(coords=("shell256",), batch=1, shape=(256, 256, 256), k=3,

@@ -110,6 +110,10 @@ def lib():
             L.spc_conv_fwd_fused.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
                                              _i32, _p, ctypes.c_float, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd_fused.restype = _i32
+            L.spc_maxpool_fwd.argtypes = [_p, _p, _p, _i32, _i64, _i64, _i32, _i32, _p, _p, _p]
+            L.spc_maxpool_fwd.restype = _i32
+            L.spc_maxpool_dgrad.argtypes = [_p, _p, _p, _i32, _i64, _i64, _i32, _i32, _p, _p]
+            L.spc_maxpool_dgrad.restype = _i32
             L.spc_conv_inverse.argtypes = [_p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32, _i32,
                                            _p, _p, _p, _sz, _p]
             L.spc_conv_inverse.restype = _i32
@@ -313,6 +317,39 @@ def spc_conv_fwd_fused(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Te
                                     0 if ws is None else ws.numel(), _stream(x.device))
     _check(code, "spc_conv_fwd_fused")
     return y
+
+
+def spc_maxpool_fwd(x: torch.Tensor, imap: torch.Tensor, mask: Optional[torch.Tensor] = None,
+                    with_arg: bool = True, out: Optional[torch.Tensor] = None,
+                    arg: Optional[torch.Tensor] = None):
+    """Sparse max pool on a strided map imap [K, N_out]: returns (y [N_out, C], arg) where
+    arg [N_out, C] uint8 holds the offset each channel took (None unless with_arg)."""
+    x = _cuda(x, "x")
+    m = _cuda(imap, "imap")
+    K, n_out = m.shape
+    c = x.shape[1]
+    y = torch.empty((n_out, c), dtype=x.dtype, device=x.device) if out is None else out
+    if with_arg and arg is None:
+        arg = torch.empty((n_out, c), dtype=torch.uint8, device=x.device)
+    code = lib().spc_maxpool_fwd(_ptr(x), _ptr(m), _ptr(mask), K, x.shape[0], n_out, c,
+                                 _DTYPES[x.dtype], _ptr(y), _ptr(arg if with_arg else None),
+                                 _stream(x.device))
+    _check(code, "spc_maxpool_fwd")
+    return y, (arg if with_arg else None)
+
+
+def spc_maxpool_dgrad(dy: torch.Tensor, imap_t: torch.Tensor, arg: torch.Tensor,
+                      out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Gradient of spc_maxpool_fwd through the transposed map imap_t [K, N_in]."""
+    dy = _cuda(dy, "dy")
+    mt = _cuda(imap_t, "imap_t")
+    K, n_in = mt.shape
+    c = dy.shape[1]
+    dx = torch.empty((n_in, c), dtype=dy.dtype, device=dy.device) if out is None else out
+    code = lib().spc_maxpool_dgrad(_ptr(dy), _ptr(mt), _ptr(_cuda(arg, "arg")), K, n_in,
+                                   dy.shape[0], c, _DTYPES[dy.dtype], _ptr(dx), _stream(dy.device))
+    _check(code, "spc_maxpool_dgrad")
+    return dx
 
 
 def spc_conv_inverse(y: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],

@@ -305,6 +305,27 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
                               0.f, SPC_ACT_NONE, y, status, ws, ws_bytes, stream);
 }
 
+spc_status spc_maxpool_fwd(const void* x, const int32_t* imap, const uint32_t* mask, int32_t K,
+                           int64_t n_in, int64_t n_out, int32_t c, spc_dtype dt, void* y,
+                           uint8_t* arg, void* stream)
+{
+    if (K < 1 || K > 254 || n_in < 0 || n_out < 0 || c < 0 || !dtype_ok(dt)) return SPC_ERR_INVALID_ARG;
+    if (mask && K > 32) return SPC_ERR_INVALID_ARG;
+    if (n_out > 0 && c > 0 && (!imap || !y || (n_in > 0 && !x))) return SPC_ERR_INVALID_ARG;
+    if (n_in > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    return maxpool_fwd(x, imap, mask, K, n_in, n_out, c, dt, y, arg, static_cast<cudaStream_t>(stream));
+}
+
+spc_status spc_maxpool_dgrad(const void* dy, const int32_t* imap_t, const uint8_t* arg, int32_t K,
+                             int64_t n_in, int64_t n_out, int32_t c, spc_dtype dt, void* dx,
+                             void* stream)
+{
+    if (K < 1 || K > 254 || n_in < 0 || n_out < 0 || c < 0 || !dtype_ok(dt)) return SPC_ERR_INVALID_ARG;
+    if (n_in > 0 && c > 0 && (!imap_t || !dx || (n_out > 0 && (!dy || !arg)))) return SPC_ERR_INVALID_ARG;
+    if (n_in > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    return maxpool_dgrad(dy, imap_t, arg, K, n_in, n_out, c, dt, dx, static_cast<cudaStream_t>(stream));
+}
+
 spc_status spc_conv_inverse(const void* y, const void* w, const void* bias, const int32_t* imap_t,
                             int32_t K, int64_t n_y, int64_t n_out, int32_t cy, int32_t cout,
                             spc_dtype dt, spc_precision prec, void* out, int32_t* status, void* ws,

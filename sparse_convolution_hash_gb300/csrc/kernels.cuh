@@ -57,6 +57,14 @@ spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const Pro
                      HashTable t, int32_t* imap, int32_t* imap_t, int32_t* pair_count,
                      uint32_t* mask, int32_t* status, cudaStream_t st);
 
+// Sparse max pooling on a strided map (maxpool.cu).
+spc_status maxpool_fwd(const void* x, const int32_t* imap, const uint32_t* mask, int32_t K,
+                       int64_t n_in, int64_t n_out, int32_t c, spc_dtype dt, void* y, uint8_t* arg,
+                       cudaStream_t st);
+spc_status maxpool_dgrad(const void* dy, const int32_t* imap_t, const uint8_t* arg, int32_t K,
+                         int64_t n_in, int64_t n_out, int32_t c, spc_dtype dt, void* dx,
+                         cudaStream_t st);
+
 // ------------------------------------------------------ strided output coords
 size_t outcoords_ws_bytes(int64_t n_in, int32_t K);
 spc_status strided_out_coords(const int32_t* coords, int64_t n_in, const ProbeGeom& g,

@@ -123,6 +123,15 @@ def test_argument_errors_return_before_any_work(L):
     assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
               4, 8, 8, 0, 0, ctypes.c_void_p(512), 1.0, 1, ctypes.c_void_p(512), None, None, 0,
               None) == E
+    # max pool: offsets beyond the uint8 argmax, a mask with K > 32, a missing map
+    assert L.spc_maxpool_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, 255, 4, 4, 8, 0,
+                             ctypes.c_void_p(512), None, None) == E
+    assert L.spc_maxpool_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), 125,
+                             4, 4, 8, 0, ctypes.c_void_p(512), None, None) == E
+    assert L.spc_maxpool_fwd(ctypes.c_void_p(256), None, None, 27, 4, 4, 8, 0,
+                             ctypes.c_void_p(512), None, None) == E
+    assert L.spc_maxpool_dgrad(ctypes.c_void_p(256), None, ctypes.c_void_p(256), 27, 4, 4, 8, 0,
+                               ctypes.c_void_p(512), None) == E
     # inverse conv: the transposed map is required; bad dtype and misaligned weight rejected
     assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, 27, 4, 4,
                               8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0, None) == E

@@ -187,6 +187,34 @@ def test_inverse_conv_strided(dtype, cy, cout):
     assert normwise(to_np(dw), oracle.conv_wgrad(y, dout, imap_t_ref)) < tol
 
 
+@pytest.mark.parametrize("ks,stride,pad", [(3, 2, 1), (2, 2, 0)])
+@pytest.mark.parametrize("dtype,c", [("bf16", 64), ("f32", 16), ("f16", 24), ("f16", 7)])
+def test_maxpool(ks, stride, pad, dtype, c):
+    """Max pool on the 2,000-voxel set: values bit-exact (a max is exact in any
+    precision), argmax offsets exact, gradient within the dtype's tolerance."""
+    w = scenes.workload("uniform32_strided_bf16")
+    coords = w["coords"]
+    d = dev()
+    dc = torch.from_numpy(coords).to(d)
+    oc, _ = spc.spc_strided_out_coords(dc, 1, (32, 32, 32), ks, stride, pad, 1)
+    m = spc.spc_build_indice_map(dc, 1, (32, 32, 32), ksize=ks, stride=stride, pad=pad, subm=False,
+                                 out_coords=oc, with_transpose=True)
+    spc.check_status(m["status"])
+    oc_ref = oracle.strided_out_coords(coords, 1, (32, 32, 32), ks, stride, pad, 1)
+    imap_ref, _, _ = oracle.strided_map(coords, oc_ref, 1, (32, 32, 32), ks, stride, pad, 1)
+    g = np.random.default_rng(ks * 100 + c)
+    x = rand_tensor(g, (coords.shape[0], c), dtype)
+    y_ref, arg_ref = oracle.maxpool_fwd(x, imap_ref)
+    for mask in (None, m["mask"]):
+        y, arg = spc.spc_maxpool_fwd(x.to(d), m["imap"], mask)
+        assert np.array_equal(to_np(y), y_ref)
+        assert np.array_equal(arg.cpu().numpy(), arg_ref)
+    dy = rand_tensor(g, (oc.shape[0], c), dtype)
+    dx = spc.spc_maxpool_dgrad(dy.to(d), m["imap_t"], arg)
+    assert normwise(to_np(dx), oracle.maxpool_dgrad(dy, imap_ref, arg_ref, coords.shape[0])) < \
+        TOL[(dtype, "exact")]
+
+
 @pytest.mark.parametrize("name", ["lidar_subm_f16", "shell256_subm_bf16", "shell256_k1_bf16"])
 def test_forward_workloads_sampled(name):
     w = scenes.workload(name)

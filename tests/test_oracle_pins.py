@@ -307,6 +307,38 @@ def test_fused_epilogue_vs_dense_conv3d_relu():
                                atol=1e-12)
 
 
+@pytest.mark.parametrize("shape,ks,stride,pad,batch", [
+    ((8, 9, 10), (3, 3, 3), (2, 2, 2), (1, 1, 1), 2),
+    ((9, 8, 7), (2, 2, 2), (2, 2, 2), (0, 0, 0), 1),
+])
+def test_maxpool_vs_dense_max_pool3d(shape, ks, stride, pad, batch):
+    """Sparse max pool = torch's dense max_pool3d over a grid holding -inf at empty
+    cells, read at the strided output set; its gradient = torch autograd's."""
+    g = np.random.default_rng(41)
+    coords = rand_coords(g, 120, batch, shape)
+    c = 5
+    x = g.standard_normal((120, c))
+    oc = oracle.strided_out_coords(coords, batch, shape, ks, stride, pad, 1)
+    imap, _, _ = oracle.strided_map(coords, oc, batch, shape, ks, stride, pad, 1, False)
+    y, arg = oracle.maxpool_fwd(x, imap)
+    t = torch.as_tensor(coords, dtype=torch.long)
+    xt = torch.as_tensor(x).clone().requires_grad_(True)
+    # scatter x into the -inf grid differentiably
+    flat = torch.full((batch * c * int(np.prod(shape)),), float("-inf"), dtype=torch.float64)
+    cell = ((t[:, 0] * c)[:, None] + torch.arange(c)[None, :]) * int(np.prod(shape)) + \
+        (((t[:, 1] * shape[1] + t[:, 2]) * shape[2]) + t[:, 3])[:, None]
+    dense = flat.index_put((cell.reshape(-1),), xt.reshape(-1)).reshape((batch, c) + tuple(shape))
+    pooled = F.max_pool3d(dense, ks, stride=stride, padding=pad)
+    to = torch.as_tensor(oc, dtype=torch.long)
+    at = pooled[to[:, 0], :, to[:, 1], to[:, 2], to[:, 3]]
+    np.testing.assert_array_equal(y, at.detach().numpy())
+    dy = g.standard_normal(at.shape)
+    at.backward(torch.as_tensor(dy))
+    np.testing.assert_allclose(oracle.maxpool_dgrad(dy, imap, arg, 120), xt.grad.numpy(),
+                               rtol=1e-12, atol=1e-12)
+    assert (arg < 255).all()  # every output of the strided set has an input
+
+
 def test_k1_is_gemm():
     g = np.random.default_rng(23)
     coords = rand_coords(g, 200, 2, (9, 9, 9))
