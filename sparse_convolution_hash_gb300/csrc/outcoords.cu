@@ -1,4 +1,10 @@
-// outcoords.cu -- output coordinate set of a strided sparse conv by sort + unique.
+// outcoords.cu -- output coordinate set of a strided sparse conv.
+//
+// When a bitmap of the output grid fits in the space the sort below keeps for
+// its keys (one bit per output cell against 16 bytes per candidate), each
+// candidate sets its cell's bit with an atomic OR instead; per-block popcounts,
+// one scan and a write of the set bits in order give the same sorted, unique
+// set in five launches.  Otherwise:
 //
 // Every (input voxel, kernel offset) pair that lands exactly on an output cell
 // (i + pad - k*dil divisible by the stride, quotient inside the output grid)
@@ -82,6 +88,145 @@ k_candidates(const int4* __restrict__ coords, int64_t n, OutGeom g,
                 keys[basepos + __popc(bal & lanemask_lt())] = key;
             }
         }
+    }
+}
+
+// Bitmap path: every candidate cell of every input voxel sets its bit.  Small
+// grids (SMEM) mark a block-private copy in shared memory and merge its
+// nonzero words once; large grids OR straight into global memory, one atomic
+// per distinct word per warp (lanes hitting the same word combine first).
+constexpr int kSmemWords = 8192;  // 32 KB: output grids of up to 262,144 cells
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kThreads)
+k_bm_mark(const int4* __restrict__ coords, int64_t n, OutGeom g, uint32_t* __restrict__ bm,
+          int64_t words, int32_t* __restrict__ status)
+{
+    __shared__ uint32_t s_bm[SMEM ? kSmemWords : 1];
+    if (SMEM) {
+        for (int64_t j = threadIdx.x; j < words; j += blockDim.x) s_bm[j] = 0u;
+        __syncthreads();
+    }
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // every lane runs the same number of rounds, so the warp stays converged
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < n; base += stride) {
+        const int64_t i = base + threadIdx.x;
+        bool valid = i < n;
+        int4 c = make_int4(0, 0, 0, 0);
+        if (valid) {
+            c = coords[i];
+            if (c.x < 0 || c.x >= g.batch || c.y < 0 || c.y >= g.in_shape[0] || c.z < 0 ||
+                c.z >= g.in_shape[1] || c.w < 0 || c.w >= g.in_shape[2]) {
+                set_status(status, SPC_ERR_COORD_RANGE);
+                valid = false;
+            }
+        }
+        const int p[3] = {c.y, c.z, c.w};
+        for (int k = 0; k < g.K; ++k) {
+            const int ka[3] = {k / (g.ksize[2] * g.ksize[1]), (k / g.ksize[2]) % g.ksize[1],
+                               k % g.ksize[2]};
+            bool ok = valid;
+            int o[3];
+#pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                const int t = p[a] + g.pad[a] - ka[a] * g.dil[a];
+                o[a] = t >= 0 ? t / g.stride[a] : -1;
+                ok = ok && t >= 0 && (t - o[a] * g.stride[a]) == 0 && o[a] < g.out_shape[a];
+            }
+            const unsigned long long key =
+                ok ? (((unsigned long long)c.x * g.out_shape[0] + (unsigned)o[0]) * g.out_shape[1] +
+                      (unsigned)o[1]) * g.out_shape[2] + (unsigned)o[2]
+                   : 0ull;
+            const uint32_t bit = ok ? 1u << (key & 31) : 0u;
+            if (SMEM) {
+                if (ok) atomicOr(&s_bm[key >> 5], bit);
+            } else {
+                // lanes of the same word OR their bits; the lowest of them writes
+                const unsigned long long word = ok ? key >> 5 : ~0ull;
+                const uint32_t same = __match_any_sync(FULL_MASK, word);
+                const uint32_t bits = __reduce_or_sync(same, bit);
+                if (ok && (threadIdx.x & 31) == __ffs(same) - 1) atomicOr(&bm[word], bits);
+            }
+        }
+    }
+    if (SMEM) {
+        __syncthreads();
+        for (int64_t j = threadIdx.x; j < words; j += blockDim.x)
+            if (s_bm[j]) atomicOr(&bm[j], s_bm[j]);
+    }
+}
+
+// Set bits of each block's kThreads words (one word per thread: a word can
+// hold 32 output cells, so the write below is spread over as many threads).
+__global__ void __launch_bounds__(kThreads)
+k_bm_count(const uint32_t* __restrict__ bm, int64_t words, uint32_t* __restrict__ blocksum)
+{
+    __shared__ uint32_t s_sum;
+    if (threadIdx.x == 0) s_sum = 0;
+    __syncthreads();
+    const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    uint32_t c = idx < words ? __popc(bm[idx]) : 0u;
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL_MASK, c, d);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&s_sum, c);
+    __syncthreads();
+    if (threadIdx.x == 0) blocksum[blockIdx.x] = s_sum;
+}
+
+// Decodes the set bits, in order, at their scanned positions (thread j of a
+// block owns word j of the block's words, so the block scan keeps the order).
+__global__ void __launch_bounds__(kThreads)
+k_bm_write(const uint32_t* __restrict__ bm, int64_t words, const uint32_t* __restrict__ blockoff,
+           const unsigned long long* __restrict__ total, OutGeom g, int4* __restrict__ out,
+           int64_t cap, int64_t* __restrict__ n_out, int32_t* __restrict__ status)
+{
+    __shared__ uint32_t s_warp[kThreads / 32];
+    const int64_t wi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    uint32_t bits = wi < words ? bm[wi] : 0u;
+    const uint32_t cnt = __popc(bits);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t inc = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(FULL_MASK, inc, d);
+        if (lane >= d) inc += t;
+    }
+    if (lane == 31) s_warp[w] = inc;
+    __syncthreads();
+    uint32_t wbase = 0;
+    for (int i = 0; i < w; ++i) wbase += s_warp[i];
+    int64_t pos = (int64_t)blockoff[blockIdx.x] + wbase + inc - cnt;
+    const unsigned W = (unsigned)g.out_shape[2], H = (unsigned)g.out_shape[1], D = (unsigned)g.out_shape[0];
+    while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (pos < cap) {
+            const unsigned long long key = (unsigned long long)wi * 32ull + (unsigned)b;
+            int4 c;
+            if (key <= 0xFFFFFFFFull) {  // 32-bit division when the cell index fits
+                unsigned k32 = (unsigned)key;
+                c.w = (int)(k32 % W);
+                k32 /= W;
+                c.z = (int)(k32 % H);
+                k32 /= H;
+                c.y = (int)(k32 % D);
+                c.x = (int)(k32 / D);
+            } else {
+                unsigned long long k64 = key;
+                c.w = (int)(k64 % W);
+                k64 /= W;
+                c.z = (int)(k64 % H);
+                k64 /= H;
+                c.y = (int)(k64 % D);
+                c.x = (int)(k64 / D);
+            }
+            out[pos] = c;
+        }
+        ++pos;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const int64_t t = (int64_t)*total;
+        *n_out = t;
+        if (t > cap) set_status(status, SPC_ERR_CAPACITY);
     }
 }
 
@@ -336,6 +481,31 @@ spc_status strided_out_coords(const int32_t* coords, int64_t n_in, const ProbeGe
         return SPC_OK;
     }
     const int64_t ncand = cand_max(n_in, pg.K);
+    const int64_t words = ceil_div(total_cells, (int64_t)32);
+    if (words <= 2 * ncand) {
+        // the bitmap takes the first key buffer, its block sums the second
+        uint32_t* bm = reinterpret_cast<uint32_t*>(w.keys_a);
+        uint32_t* bsum = reinterpret_cast<uint32_t*>(w.keys_b);
+        const int nb = (int)ceil_div(words, (int64_t)kThreads);
+        SPC_CUDA_TRY(cudaMemsetAsync(bm, 0, sizeof(uint32_t) * (size_t)words, st));
+        const int grid = (int)std::min<int64_t>(ceil_div(n_in, kThreads), 8 * sm_count());
+        if (words <= kSmemWords)
+            k_bm_mark<true><<<grid, kThreads, 0, st>>>(reinterpret_cast<const int4*>(coords), n_in,
+                                                       g, bm, words, status);
+        else
+            k_bm_mark<false><<<grid, kThreads, 0, st>>>(reinterpret_cast<const int4*>(coords), n_in,
+                                                        g, bm, words, status);
+        SPC_LAUNCH_CHECK();
+        k_bm_count<<<nb, kThreads, 0, st>>>(bm, words, bsum);
+        SPC_LAUNCH_CHECK();
+        k_scan_exclusive<<<1, kScanThreads, 0, st>>>(bsum, nb, w.counter + 1);
+        SPC_LAUNCH_CHECK();
+        k_bm_write<<<nb, kThreads, 0, st>>>(bm, words, bsum, w.counter + 1, g,
+                                            reinterpret_cast<int4*>(out_coords), cap, n_out,
+                                            status);
+        SPC_LAUNCH_CHECK();
+        return SPC_OK;
+    }
     const int nblocks = (int)ceil_div(ncand, kTile);
     {
         const int grid = (int)std::min<int64_t>(ceil_div(n_in, kThreads), 8 * sm_count());

@@ -115,6 +115,10 @@ def check_strided(coords, batch, shape, ks, st, pd, dl):
     (700, 1, (16, 9, 12), (3, 2, 3), (2, 2, 1), (0, 1, 1), (1, 1, 2)),
     (5000, 3, (20, 20, 20), 2, 2, 0, 1),
     (4097, 1, (33, 31, 29), 3, 3, 1, 1),
+    # few voxels in a large grid: the output-grid bitmap would not fit the
+    # candidates' key space, so these take the radix-sort path
+    (3, 1, (200, 210, 190), 3, 2, 1, 1),
+    (40, 2, (128, 128, 128), 2, 2, 0, 1),
 ])
 def test_strided_small(n, batch, shape, ks, st, pd, dl):
     g = np.random.default_rng(n + 7)
