@@ -66,8 +66,8 @@ DESCRIPTIONS = {
                                 "ReLU (relu(conv(x) + x)), 4 x 192^3 shells, bf16 64->64",
     "shell256_maxpool_bf16": "SparseMaxPool3d k2 s2 forward (with argmax) + input gradient "
                              "(maps built once), 256^3 shell, bf16 128 channels",
-    "shell256_inverse_bf16": "SparseInverseConv3d of a k3 s2 p1 conv (maps built once), 256^3 "
-                             "shell, bf16 128->128",
+    "shell256_inverse_bf16": "SparseInverseConv3d of a k3 s2 p1 conv (maps and row order "
+                             "built once), 256^3 shell, bf16 128->128",
 }
 ELEM = {"f32": 4, "f16": 2, "bf16": 2}
 
@@ -304,10 +304,13 @@ class Case:
             nbw = int(B.lib().spc_conv_workspace_size(K, n_out, n, cin, cout, B._DTYPES[self.x.dtype]))
             self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
             self.train = False
+            # rows grouped by offset mask, saved with the maps (spc_map_row_order)
+            self.mask_t, self.perm = spc.spc_map_row_order(self.m["imap_t"])
             self.phases.append(Phase(
                 "inverse", lambda: spc.spc_conv_inverse(self.yin, self.wt, self.bias, self.m["imap_t"],
                                                         precision=self.prec, out=self.y,
-                                                        status=self.status, ws=self.conv_ws),
+                                                        status=self.status, ws=self.conv_ws,
+                                                        mask_t=self.mask_t, perm=self.perm),
                 "conv", s * n_out * cin + s * n * cout + s * K * cin * cout + 4 * P,
                 2.0 * P * cin * cout, kernels=self.fwd_kernel(),
                 launches=2 if "tcgen05" in self.fwd_kernel() else 1))

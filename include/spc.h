@@ -277,15 +277,37 @@ SPC_API spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* 
  *  w      [K, cy, cout] of dtype dt.   bias [cout] or NULL.
  *  imap_t [K, n_out] int32: the strided conv's transposed map from
  *         spc_build_indice_map (imap_t[k, i] = o exactly when imap[k, o] = i).
+ *  mask_t, perm  [n_out] uint32 / int32 from spc_map_row_order(imap_t), or
+ *         NULL (K <= 32 when given).  With them the tensor-core kernel computes
+ *         its row tiles in an order that groups rows using the same offsets,
+ *         and a tile runs only those offsets; the result is the same.
  *  out    [n_out, cout] of dtype dt out: rows of the strided conv's input set.
  *  ws     spc_conv_workspace_size(K, n_y, n_out, cy, cout, dt) bytes.
  *  Errors and alignment as for spc_conv_fwd.
  */
 SPC_API spc_status spc_conv_inverse(const void* y, const void* w, const void* bias,
-                                    const int32_t* imap_t, int32_t K, int64_t n_y, int64_t n_out,
+                                    const int32_t* imap_t, const uint32_t* mask_t,
+                                    const int32_t* perm, int32_t K, int64_t n_y, int64_t n_out,
                                     int32_t cy, int32_t cout, spc_dtype dt, spc_precision prec,
                                     void* out, int32_t* status, void* ws, size_t ws_bytes,
                                     void* stream);
+
+/* spc_map_row_order -- the rows of a map [K, n] grouped by offset mask.
+ * mask[i] gets bit k when map[k, i] != -1, and perm lists the rows sorted by
+ * mask (stable: rows keep their order within a group).  For the transposed map
+ * of a strided conv the groups are the stride's residue classes of the input
+ * coordinates, each using only a few offsets, so a tile of grouped rows skips
+ * most of the K offsets that a tile of consecutive rows would run (no
+ * counterpart on the pages: it is how this library feeds spc_conv_inverse).
+ * Computed once per map, like the map itself.
+ *
+ *  map   [K, n] int32, K <= 32.   mask [n] uint32 out or NULL.
+ *  perm  [n] int32 out: a permutation of 0 .. n-1.
+ *  ws    spc_map_row_order_workspace_size(n) bytes.
+ */
+SPC_API size_t spc_map_row_order_workspace_size(int64_t n);
+SPC_API spc_status spc_map_row_order(const int32_t* map, int32_t K, int64_t n, uint32_t* mask,
+                                     int32_t* perm, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------ pooling
  * spc_maxpool_fwd -- y[o, c] = max over the pairs imap[k, o] = i of x[i, c]

@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     SPC_ACT_NONE,
     SPC_ACT_RELU,
     spc_conv_inverse,
+    spc_map_row_order,
     spc_maxpool_fwd,
     spc_maxpool_dgrad,
     spc_conv_wgrad,

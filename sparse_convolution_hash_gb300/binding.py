@@ -114,8 +114,12 @@ def lib():
             L.spc_maxpool_fwd.restype = _i32
             L.spc_maxpool_dgrad.argtypes = [_p, _p, _p, _i32, _i64, _i64, _i32, _i32, _p, _p]
             L.spc_maxpool_dgrad.restype = _i32
-            L.spc_conv_inverse.argtypes = [_p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32, _i32,
-                                           _p, _p, _p, _sz, _p]
+            L.spc_conv_inverse.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
+                                           _i32, _p, _p, _p, _sz, _p]
+            L.spc_map_row_order_workspace_size.argtypes = [_i64]
+            L.spc_map_row_order_workspace_size.restype = _sz
+            L.spc_map_row_order.argtypes = [_p, _i32, _i64, _p, _p, _p, _sz, _p]
+            L.spc_map_row_order.restype = _i32
             L.spc_conv_inverse.restype = _i32
             L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _i32, _i64, _i64, _i32, _i32,
                                          _i32, _i32, _p, _p, _p, _sz, _p]
@@ -352,12 +356,29 @@ def spc_maxpool_dgrad(dy: torch.Tensor, imap_t: torch.Tensor, arg: torch.Tensor,
     return dx
 
 
+def spc_map_row_order(map_: torch.Tensor, ws: Optional[torch.Tensor] = None):
+    """(mask [n] uint32, perm [n] int32): rows of map [K, n] grouped by offset mask."""
+    m = _cuda(map_, "map")
+    K, n = m.shape
+    mask = torch.empty(n, dtype=torch.int32, device=m.device)
+    perm = torch.empty(n, dtype=torch.int32, device=m.device)
+    nbytes = int(lib().spc_map_row_order_workspace_size(n))
+    if ws is None or ws.numel() < nbytes:
+        ws = _workspace(nbytes, m.device)
+    code = lib().spc_map_row_order(_ptr(m), K, n, _ptr(mask), _ptr(perm), _ptr(ws), ws.numel(),
+                                   _stream(m.device))
+    _check(code, "spc_map_row_order")
+    return mask, perm
+
+
 def spc_conv_inverse(y: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
                      imap_t: torch.Tensor, precision: int = SPC_PREC_EXACT,
                      out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                     ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+                     ws: Optional[torch.Tensor] = None, mask_t: Optional[torch.Tensor] = None,
+                     perm: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Inverse of a strided conv through its transposed map imap_t [K, N_in]:
-    out[i] = bias + sum over pairs imap_t[k, i] = o of y[o] W[k]; out [N_in, Cout]."""
+    out[i] = bias + sum over pairs imap_t[k, i] = o of y[o] W[k]; out [N_in, Cout].
+    mask_t / perm from spc_map_row_order(imap_t) let the kernel skip unused offsets."""
     y = _cuda(y, "y")
     w = _cuda(w, "w").to(y.dtype)
     b = _cuda(bias, "bias").to(y.dtype) if bias is not None else None
@@ -369,9 +390,10 @@ def spc_conv_inverse(y: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tens
     nbytes = int(lib().spc_conv_workspace_size(K, y.shape[0], n_out, cy, cout, dt))
     if nbytes and (ws is None or ws.numel() < nbytes):
         ws = _workspace(nbytes, y.device)
-    code = lib().spc_conv_inverse(_ptr(y), _ptr(w), _ptr(b), _ptr(m), K, y.shape[0], n_out, cy,
-                                  cout, dt, precision, _ptr(o), _ptr(status), _ptr(ws),
-                                  0 if ws is None else ws.numel(), _stream(y.device))
+    code = lib().spc_conv_inverse(_ptr(y), _ptr(w), _ptr(b), _ptr(m), _ptr(mask_t), _ptr(perm), K,
+                                  y.shape[0], n_out, cy, cout, dt, precision, _ptr(o),
+                                  _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
+                                  _stream(y.device))
     _check(code, "spc_conv_inverse")
     return o
 

@@ -232,11 +232,14 @@ spc_status run_gather(const GatherGemm& p, spc_dtype dt, cudaStream_t st)
 
 }  // namespace
 
-spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias, const int32_t* imap,
-                              const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
-                              int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec,
-                              const void* residual, float add_scale, spc_activation act, void* y,
-                              int32_t* status, void* ws, size_t ws_bytes, void* stream)
+namespace {
+// The forward of every entry point; perm (or NULL) orders the tensor-core
+// kernel's tiles (the CUDA-core kernels own one row per thread and ignore it).
+spc_status conv_fwd_impl(const void* x, const void* w, const void* bias, const int32_t* imap,
+                         const uint32_t* mask, const int32_t* perm, int32_t K, int64_t n_in,
+                         int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec,
+                         const void* residual, float add_scale, spc_activation act, void* y,
+                         int32_t* status, void* ws, size_t ws_bytes, void* stream)
 {
     spc_status s = check_conv(x, w, y, K, n_in, n_out, cin, cout, dt);
     if (s != SPC_OK) return s;
@@ -287,6 +290,7 @@ spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias, co
         a.cred = cin;
         a.n_total = cout;
         a.mirror = 0;
+        a.perm = perm;
         a.residual = residual;
         a.add_scale = add_scale;
         a.act = (int32_t)act;
@@ -296,13 +300,36 @@ spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias, co
     return run_gather(p, dt, st);
 }
 
+}  // namespace
+
+spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias, const int32_t* imap,
+                              const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
+                              int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec,
+                              const void* residual, float add_scale, spc_activation act, void* y,
+                              int32_t* status, void* ws, size_t ws_bytes, void* stream)
+{
+    return conv_fwd_impl(x, w, bias, imap, mask, nullptr, K, n_in, n_out, cin, cout, dt, prec,
+                         residual, add_scale, act, y, status, ws, ws_bytes, stream);
+}
+
 spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const int32_t* imap,
                         const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
                         int32_t cout, spc_dtype dt, spc_precision prec, void* y, int32_t* status,
                         void* ws, size_t ws_bytes, void* stream)
 {
-    return spc_conv_fwd_fused(x, w, bias, imap, mask, K, n_in, n_out, cin, cout, dt, prec, nullptr,
-                              0.f, SPC_ACT_NONE, y, status, ws, ws_bytes, stream);
+    return conv_fwd_impl(x, w, bias, imap, mask, nullptr, K, n_in, n_out, cin, cout, dt, prec,
+                         nullptr, 0.f, SPC_ACT_NONE, y, status, ws, ws_bytes, stream);
+}
+
+size_t spc_map_row_order_workspace_size(int64_t n) { return n < 0 ? 0 : row_order_ws_bytes(n); }
+
+spc_status spc_map_row_order(const int32_t* map, int32_t K, int64_t n, uint32_t* mask,
+                             int32_t* perm, void* ws, size_t ws_bytes, void* stream)
+{
+    if (K < 1 || K > 32 || n < 0) return SPC_ERR_INVALID_ARG;
+    if (n > 0 && (!map || !perm)) return SPC_ERR_INVALID_ARG;
+    if (n > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    return map_row_order(map, K, n, mask, perm, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 spc_status spc_maxpool_fwd(const void* x, const int32_t* imap, const uint32_t* mask, int32_t K,
@@ -327,15 +354,17 @@ spc_status spc_maxpool_dgrad(const void* dy, const int32_t* imap_t, const uint8_
 }
 
 spc_status spc_conv_inverse(const void* y, const void* w, const void* bias, const int32_t* imap_t,
-                            int32_t K, int64_t n_y, int64_t n_out, int32_t cy, int32_t cout,
-                            spc_dtype dt, spc_precision prec, void* out, int32_t* status, void* ws,
+                            const uint32_t* mask_t, const int32_t* perm, int32_t K, int64_t n_y,
+                            int64_t n_out, int32_t cy, int32_t cout, spc_dtype dt,
+                            spc_precision prec, void* out, int32_t* status, void* ws,
                             size_t ws_bytes, void* stream)
 {
     // the inverse conv gathers through the transposed map: rows of the strided
     // conv's input set are its outputs, rows of its output set its inputs
     if (n_out > 0 && !imap_t) return SPC_ERR_INVALID_ARG;
-    return spc_conv_fwd(y, w, bias, imap_t, nullptr, K, n_y, n_out, cy, cout, dt, prec, out, status,
-                        ws, ws_bytes, stream);
+    if ((mask_t || perm) && K > 32) return SPC_ERR_INVALID_ARG;
+    return conv_fwd_impl(y, w, bias, imap_t, mask_t, perm, K, n_y, n_out, cy, cout, dt, prec,
+                         nullptr, 0.f, SPC_ACT_NONE, out, status, ws, ws_bytes, stream);
 }
 
 spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
@@ -387,6 +416,7 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
         a.cred = cout;
         a.n_total = cin;
         a.mirror = p.mirror;
+        a.perm = nullptr;
         a.residual = nullptr;
         a.add_scale = 0.f;
         a.act = 0;

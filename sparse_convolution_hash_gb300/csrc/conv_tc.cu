@@ -132,8 +132,10 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
     ptx::tc_fence_after();
 
     // union of the tile's row masks (thread t owns row t of the tile)
-    const int64_t row = row0 + tid;
-    const bool rvalid = tid < kRowsPerCta && row < a.rows;
+    // tile row -> output row: the identity, or a caller's order that puts rows
+    // with the same offsets into the same tiles
+    const bool rvalid = tid < kRowsPerCta && row0 + tid < a.rows;
+    const int64_t row = rvalid && a.perm ? (int64_t)__ldg(a.perm + row0 + tid) : row0 + tid;
     uint32_t m = 0;
     if (tid < kRowsPerCta) {
         if (rvalid) {
@@ -279,8 +281,9 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
         // (w/4)%MT, and column group w/(4 MT) of the tile's BN
         constexpr int kGroups = NW / (4 * MT), kGroupCols = BN / kGroups;
         const int quarter = warp & 3, half = (warp >> 2) % MT, cgrp = warp / (4 * MT);
-        const int64_t erow = row0 + half * kHalf + quarter * 32 + lane;
-        const bool evalid = erow < a.rows;
+        const int64_t trow = row0 + half * kHalf + quarter * 32 + lane;
+        const bool evalid = trow < a.rows;
+        const int64_t erow = evalid && a.perm ? (int64_t)__ldg(a.perm + trow) : trow;
         if (aborted) {
             if (tid == 0) set_status(a.status, SPC_ERR_TIMEOUT);
         } else {

@@ -65,6 +65,16 @@ spc_status maxpool_dgrad(const void* dy, const int32_t* imap_t, const uint8_t* a
                          int64_t n_in, int64_t n_out, int32_t c, spc_dtype dt, void* dx,
                          cudaStream_t st);
 
+// Row order of a map grouped by offset mask (rows.cu).
+size_t row_order_ws_bytes(int64_t n);
+spc_status map_row_order(const int32_t* map, int32_t K, int64_t n, uint32_t* mask, int32_t* perm,
+                         void* ws, size_t ws_bytes, cudaStream_t st);
+// Stable LSD radix sort of n 64-bit keys on bits [lo_bit, hi_bit) (outcoords.cu);
+// keys end in `a` (b is scratch); counter holds n on the device.
+size_t radix_ws_bytes(int64_t n);
+spc_status radix_sort_keys(unsigned long long* a, unsigned long long* b, const unsigned long long* counter,
+                           int64_t n, int lo_bit, int hi_bit, void* ws, cudaStream_t st);
+
 // ------------------------------------------------------ strided output coords
 size_t outcoords_ws_bytes(int64_t n_in, int32_t K);
 spc_status strided_out_coords(const int32_t* coords, int64_t n_in, const ProbeGeom& g,
@@ -120,6 +130,7 @@ struct TcArgs {
     const void* residual;   // fused epilogue, as in GatherGemm
     float add_scale;
     int32_t act;
+    const int32_t* perm;    // tile row r computes output row perm[r] (NULL: r)
 };
 bool conv_tc_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt, spc_precision prec);
 size_t conv_tc_weight_bytes(int32_t K, int32_t cin, int32_t cout, spc_dtype dt);

@@ -446,6 +446,35 @@ size_t carve(int64_t n_in, int32_t K, char* base, OutWs* w)
 
 size_t outcoords_ws_bytes(int64_t n_in, int32_t K) { return carve(n_in, K, nullptr, nullptr); }
 
+size_t radix_ws_bytes(int64_t n)
+{
+    const int64_t nblocks = ceil_div(n > 0 ? n : 1, (int64_t)kTile);
+    return align_up(sizeof(uint32_t) * (size_t)kRadix * (size_t)nblocks, 256);
+}
+
+spc_status radix_sort_keys(unsigned long long* a, unsigned long long* b, const unsigned long long* counter,
+                           int64_t n, int lo_bit, int hi_bit, void* ws, cudaStream_t st)
+{
+    if (n <= 1 || hi_bit <= lo_bit) return SPC_OK;
+    const int nblocks = (int)ceil_div(n, (int64_t)kTile);
+    uint32_t* hist = static_cast<uint32_t*>(ws);
+    unsigned long long* src = a;
+    unsigned long long* dst = b;
+    for (int shift = lo_bit; shift < hi_bit; shift += 8) {
+        k_radix_hist<<<nblocks, kThreads, 0, st>>>(src, counter, shift, hist, nblocks);
+        SPC_LAUNCH_CHECK();
+        k_scan_exclusive<<<1, kScanThreads, 0, st>>>(hist, (int64_t)kRadix * nblocks, nullptr);
+        SPC_LAUNCH_CHECK();
+        k_radix_scatter<<<nblocks, kThreads, 0, st>>>(src, dst, counter, shift, hist, nblocks);
+        SPC_LAUNCH_CHECK();
+        std::swap(src, dst);
+    }
+    if (src != a)
+        SPC_CUDA_TRY(cudaMemcpyAsync(a, src, sizeof(unsigned long long) * (size_t)n,
+                                     cudaMemcpyDeviceToDevice, st));
+    return SPC_OK;
+}
+
 spc_status strided_out_coords(const int32_t* coords, int64_t n_in, const ProbeGeom& pg,
                               const int32_t out_shape[3], int32_t* out_coords, int64_t cap,
                               int64_t* n_out, int32_t* status, void* ws, size_t ws_bytes,

@@ -132,15 +132,26 @@ def test_argument_errors_return_before_any_work(L):
                              ctypes.c_void_p(512), None, None) == E
     assert L.spc_maxpool_dgrad(ctypes.c_void_p(256), None, ctypes.c_void_p(256), 27, 4, 4, 8, 0,
                                ctypes.c_void_p(512), None) == E
-    # inverse conv: the transposed map is required; bad dtype and misaligned weight rejected
-    assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, 27, 4, 4,
-                              8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0, None) == E
-    assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(256), None,
-                              ctypes.c_void_p(256), 27, 4, 4, 8, 8, 7, 0, ctypes.c_void_p(256),
-                              None, None, 0, None) == E
-    assert L.spc_conv_inverse(ctypes.c_void_p(256), ctypes.c_void_p(258), None,
-                              ctypes.c_void_p(256), 27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256),
-                              None, None, 0, None) == E
+    # inverse conv: the transposed map is required; bad dtype, misaligned weight, and a
+    # row order with K > 32 rejected
+    inv = L.spc_conv_inverse
+    assert inv(ctypes.c_void_p(256), ctypes.c_void_p(256), None, None, None, None, 27, 4, 4, 8, 8,
+               0, 0, ctypes.c_void_p(256), None, None, 0, None) == E
+    assert inv(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, None,
+               27, 4, 4, 8, 8, 7, 0, ctypes.c_void_p(256), None, None, 0, None) == E
+    assert inv(ctypes.c_void_p(256), ctypes.c_void_p(258), None, ctypes.c_void_p(256), None, None,
+               27, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0, None) == E
+    assert inv(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None,
+               ctypes.c_void_p(256), 125, 4, 4, 8, 8, 0, 0, ctypes.c_void_p(256), None, None, 0,
+               None) == E
+    # row order: K beyond the mask bits, missing output, too small a workspace
+    assert L.spc_map_row_order(ctypes.c_void_p(256), 33, 4, None, ctypes.c_void_p(256),
+                               ctypes.c_void_p(256), 1 << 20, None) == E
+    assert L.spc_map_row_order(ctypes.c_void_p(256), 27, 4, None, None, ctypes.c_void_p(256),
+                               1 << 20, None) == E
+    assert L.spc_map_row_order(ctypes.c_void_p(256), 27, 4, None, ctypes.c_void_p(256),
+                               ctypes.c_void_p(256), 8, None) == 8
+    assert L.spc_map_row_order_workspace_size(1000) >= 16 * 1000
     # the tensor-core path needs its workspace (transposed weights)
     assert L.spc_conv_workspace_size(27, 4, 4, 128, 128, binding.SPC_BF16) == 27 * 128 * 128 * 2
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256),

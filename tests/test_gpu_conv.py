@@ -175,8 +175,19 @@ def test_inverse_conv_strided(dtype, cy, cout):
     tol = TOL[(dtype, "exact")]
     out = spc.spc_conv_inverse(y.to(d), wt.to(d), b.to(d), m["imap_t"])
     assert out.shape == (n, cout)
-    assert normwise(to_np(out), oracle.conv_inverse(y, wt, b, imap_ref, n)) < tol
+    ref = oracle.conv_inverse(y, wt, b, imap_ref, n)
+    assert normwise(to_np(out), ref) < tol
     assert torch.equal(out, spc.spc_conv_inverse(y.to(d), wt.to(d), b.to(d), m["imap_t"]))
+    # rows grouped by offset mask: a permutation, masks non-decreasing along it,
+    # stable within a group, and the same result
+    mask_t, perm = spc.spc_map_row_order(m["imap_t"])
+    p_np, mk = perm.cpu().numpy(), mask_t.cpu().numpy().astype(np.uint32)
+    assert np.array_equal(np.sort(p_np), np.arange(n))
+    exp_mask = ((imap_t_ref >= 0) * (1 << np.arange(27, dtype=np.int64))[:, None]).sum(0)
+    assert np.array_equal(mk.astype(np.int64), exp_mask)
+    assert np.array_equal(p_np, np.lexsort((np.arange(n), exp_mask)))
+    out_g = spc.spc_conv_inverse(y.to(d), wt.to(d), b.to(d), m["imap_t"], mask_t=mask_t, perm=perm)
+    assert normwise(to_np(out_g), ref) < tol
     dout = rand_tensor(g, (n, cout), dtype)
     # dy[o] = sum over pairs imap[k, o] = i of W[k] dout[i]: the forward map read as transposed
     dy = spc.spc_conv_dgrad(dout.to(d), wt.to(d), m["imap"], spc.SPC_MAP_TRANSPOSED, n_y)
