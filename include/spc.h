@@ -217,7 +217,9 @@ SPC_API spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, i
  *        needs no map (lato_mlx sparse/conv.py, SubMConv3d.__call__ k=1
  *        shortcut; HYGON-AI spconv-das README, 1x1 takes the GEMM path).
  *  mask  [n_out] uint32 or NULL: the per-row offset mask from
- *        spc_build_indice_map; lets tiles skip offsets no row of theirs uses.
+ *        spc_build_indice_map; the narrow-channel kernel walks only a row's
+ *        set bits (the tensor-core kernel reads all of a row's map entries in
+ *        one burst and skips the offsets no row of its tile uses).
  *  y     [n_out, cout] of dtype dt out (fp32 accumulate, one rounding).
  *  status  device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
  *  ws    spc_conv_workspace_size(...) bytes (the tensor-core path keeps the

@@ -2,9 +2,10 @@
 // (tcgen05, accumulators in tensor memory) for wide channels.
 //
 // Output-stationary: a CTA owns 256 output rows (two 128-row MMA tiles with
-// their own accumulators, sharing every weight stage) x BN output channels.  It first ORs its rows' offset masks, so offsets that no row of
-// the tile uses are skipped, and reads its rows' map entries for the remaining
-// offsets.  The K loop then runs over (active offset, 128-byte channel chunk):
+// their own accumulators, sharing every weight stage) x BN output channels.  It
+// reads its rows' map entries in one burst and skips the offsets no row of the
+// tile uses (rows in a caller's grouped order read their masks first and load
+// only the entries they have).  The K loop then runs over (active offset, 128-byte channel chunk):
 //   warps 0-15 gather the 256 input rows of that offset with 16-byte cp.async
 //     copies straight into a 128-byte-swizzled K-major shared-memory stage (a
 //     warp instruction copies four whole 128-byte row segments; rows with no
@@ -136,19 +137,44 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
     // with the same offsets into the same tiles
     const bool rvalid = tid < kRowsPerCta && row0 + tid < a.rows;
     const int64_t row = rvalid && a.perm ? (int64_t)__ldg(a.perm + row0 + tid) : row0 + tid;
+    // Map entries of the tile's rows into s_idx, one row of s_idx per offset
+    // that some row of the tile uses.  Rows in a caller's grouped order have
+    // few offsets each: their masks are read first and only those entries are
+    // loaded.  Otherwise all K entries of a row are loaded in one burst (no
+    // dependent mask read first) and the tile's offsets are those where some
+    // row has an entry.
+    const bool by_mask = a.perm && a.mask;
+    int32_t iv[32];
     uint32_t m = 0;
     if (tid < kRowsPerCta) {
-        if (rvalid) {
-            m = a.mask ? __ldcs(a.mask + row) : kmask;  // read once: evict first
-            if (a.mask && a.mirror) m = __brev(m) >> (32 - K);
-            m &= kmask;
+        if (by_mask) {
+            if (rvalid) {
+                m = __ldcs(a.mask + row);  // read once: evict first
+                if (a.mirror) m = __brev(m) >> (32 - K);
+                m &= kmask;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                iv[k] = -1;
+                if (k < K && rvalid) {
+                    const int mk = a.mirror ? K - 1 - k : k;
+                    iv[k] = a.map ? __ldcs(a.map + (int64_t)mk * a.rows + row) : (int32_t)row;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                if (iv[k] >= a.in_rows || iv[k] < 0) iv[k] = -1;
+                m |= (iv[k] >= 0 ? 1u : 0u) << k;
+            }
         }
         const uint32_t wu = __reduce_or_sync(FULL_MASK, m);
         if (lane == 0 && wu) atomicOr(reinterpret_cast<unsigned*>(&s_ctrl[2]), wu);
     }
     __syncthreads();
+    const uint32_t uni = (uint32_t)s_ctrl[2];
     if (tid == 0) {
-        uint32_t u = (uint32_t)s_ctrl[2];
+        uint32_t u = uni;
         int n = 0;
         while (u) {
             s_active[n++] = __ffs(u) - 1;
@@ -156,29 +182,34 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
         }
         s_ctrl[0] = n;
     }
-    __syncthreads();
-    const int nact = s_ctrl[0];
-    if (tid < kRowsPerCta) {
-        // this row's map entries for the tile's active offsets (all loads in
-        // flight before the first store); misses become the out-of-range row
-        // in_rows, which the gather fills with zeros
-        int32_t iv[32];
+    if (tid < kRowsPerCta && !by_mask) {
 #pragma unroll
-        for (int ai = 0; ai < 32; ++ai) {
-            iv[ai] = -1;
-            if (ai < nact) {
-                const int k = s_active[ai];
-                if (rvalid && ((m >> k) & 1u)) {
-                    const int mk = a.mirror ? K - 1 - k : k;
-                    iv[ai] = a.map ? __ldcs(a.map + (int64_t)mk * a.rows + row) : (int32_t)row;
-                }
-            }
-        }
-#pragma unroll
-        for (int ai = 0; ai < 32; ++ai)
-            if (ai < nact) s_idx[ai * kRowsPerCta + tid] = iv[ai] < a.in_rows ? iv[ai] : -1;
+        for (int k = 0; k < 32; ++k)
+            if ((uni >> k) & 1u) s_idx[__popc(uni & ((1u << k) - 1u)) * kRowsPerCta + tid] = iv[k];
     }
     __syncthreads();
+    const int nact = s_ctrl[0];
+    if (by_mask) {
+        if (tid < kRowsPerCta) {
+            // this row's entries for the tile's active offsets, all loads in flight
+            // before the first store
+#pragma unroll
+            for (int ai = 0; ai < 32; ++ai) {
+                iv[ai] = -1;
+                if (ai < nact) {
+                    const int k = s_active[ai];
+                    if (rvalid && ((m >> k) & 1u)) {
+                        const int mk = a.mirror ? K - 1 - k : k;
+                        iv[ai] = __ldcs(a.map + (int64_t)mk * a.rows + row);
+                    }
+                }
+            }
+#pragma unroll
+            for (int ai = 0; ai < 32; ++ai)
+                if (ai < nact) s_idx[ai * kRowsPerCta + tid] = (iv[ai] >= 0 && iv[ai] < a.in_rows) ? iv[ai] : -1;
+        }
+        __syncthreads();
+    }
     const int kchunks = a.cred / S::CH;
     const int n_iter = nact * kchunks;
     const uint32_t tmem = (uint32_t)s_ctrl[3];
