@@ -459,6 +459,10 @@ spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
     // fastest of the shapes measured; the gathers are the limiting resource)
     constexpr int E = (int)sizeof(T);
     if (a.cred * E % 128 == 0) {
+        // rows in grouped order run only a few offsets per tile: smaller tiles and
+        // rings let two CTAs share an SM, so one's set-up overlaps the other's work
+        if (a.perm && a.n_total % 128 == 0) return launch_tc<T, 128, 2, 1, 8, 128>(a, st);
+        if (a.perm) return launch_tc<T, 64, 2, 1, 8, 128>(a, st);
         if (a.n_total % 128 == 0) return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
         return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
     }

@@ -153,7 +153,8 @@ def test_fused_epilogue(n, cin, cout, dtype, prec, res_scale, relu):
 
 
 @pytest.mark.parametrize("dtype,cy,cout", [("bf16", 128, 64), ("f16", 64, 64), ("f32", 16, 16),
-                                           ("bf16", 32, 32), ("bf16", 64, 16), ("f16", 24, 40)])
+                                           ("bf16", 32, 32), ("bf16", 64, 16), ("f16", 24, 40),
+                                           ("bf16", 64, 128), ("f32", 64, 192)])
 def test_inverse_conv_strided(dtype, cy, cout):
     """Inverse of the k3 s2 p1 conv on the 2,000-voxel set: output, and both
     gradients through the documented spc_conv_dgrad / spc_conv_wgrad calls."""
