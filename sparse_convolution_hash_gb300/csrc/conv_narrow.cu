@@ -66,11 +66,11 @@ constexpr int kSliceStride = CRED * COUT + 4;
 template <typename T, int CRED, int COUT>
 constexpr int kNarrowBatch = CRED * (int)sizeof(T) >= 64 ? 1 : (CRED * (int)sizeof(T) >= 32 ? 2 : 4);
 
-// Up to kBatch of the offsets left in m (lowest first, removed from m): their
-// map entries, then their neighbours' rows, all loads in flight together.
-template <typename T, int CRED, int kBatch>
-__device__ __forceinline__ void load_batch(uint32_t& m, const GatherGemm& p, int64_t r, int (&ks)[kBatch],
-                                           int32_t (&idx)[kBatch], RowVec<T, CRED> (&xv)[kBatch])
+// Up to kBatch of the offsets left in m (lowest first, removed from m) and
+// their map entries (loads in flight together).
+template <int kBatch>
+__device__ __forceinline__ void take_batch(uint32_t& m, const GatherGemm& p, int64_t r, int (&ks)[kBatch],
+                                           int32_t (&idx)[kBatch])
 {
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
@@ -85,6 +85,13 @@ __device__ __forceinline__ void load_batch(uint32_t& m, const GatherGemm& p, int
             idx[b] = p.map ? __ldcs(p.map + (int64_t)mk * p.rows + r) : (int32_t)r;
         }
     }
+}
+
+// The neighbour rows of a batch (loads in flight together).
+template <typename T, int CRED, int kBatch>
+__device__ __forceinline__ void load_rows(const GatherGemm& p, const int32_t (&idx)[kBatch],
+                                          RowVec<T, CRED> (&xv)[kBatch])
+{
 #pragma unroll
     for (int b = 0; b < kBatch; ++b)
         if (idx[b] >= 0) load_row(xv[b], static_cast<const T*>(p.in), idx[b]);
@@ -109,13 +116,16 @@ __global__ void __launch_bounds__(kThreads, (COUT <= 16 ? 4 : 2)) k_conv_narrow(
     int ks[kBatch];
     int32_t idx[kBatch];
     RowVec<T, CRED> xv[kBatch];
+    bool have_rows = false;
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) idx[b] = -1;
     if (p.mask && r < p.rows) {
         m = __ldcs(p.mask + r);  // read once: evict first
         if (p.mirror) m = __brev(m) >> (32 - K);
         m &= kmask;
-        load_batch<T, CRED, kBatch>(m, p, r, ks, idx, xv);
+        take_batch<kBatch>(m, p, r, ks, idx);
+        load_rows<T, CRED, kBatch>(p, idx, xv);
+        have_rows = true;
     }
     {
         // weights: 16-byte vector loads in global order, converted to fp32
@@ -163,14 +173,27 @@ __global__ void __launch_bounds__(kThreads, (COUT <= 16 ? 4 : 2)) k_conv_narrow(
                 m = __ldcs(p.mask + r);
                 if (p.mirror) m = __brev(m) >> (32 - K);
                 m &= kmask;
-                load_batch<T, CRED, kBatch>(m, p, r, ks, idx, xv);
+                take_batch<kBatch>(m, p, r, ks, idx);
+                have_rows = false;
             }
+            // the next batch's map entries are requested while this batch's rows
+            // load, so a row of n batches costs about n + 1 round trips, not 2n
             while (true) {
+                int ks2[kBatch];
+                int32_t idx2[kBatch];
+                const bool more = m != 0;
+                if (more) take_batch<kBatch>(m, p, r, ks2, idx2);
+                if (!have_rows) load_rows<T, CRED, kBatch>(p, idx, xv);
+                have_rows = false;
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b)
                     if (idx[b] >= 0) fma_row<T, CRED, COUT>(acc, xv[b], s_w + (size_t)ks[b] * kStr);
-                if (!m) break;
-                load_batch<T, CRED, kBatch>(m, p, r, ks, idx, xv);
+                if (!more) break;
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    ks[b] = ks2[b];
+                    idx[b] = idx2[b];
+                }
             }
         } else {
             for (int k = 0; k < K; ++k) {
