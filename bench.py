@@ -261,10 +261,15 @@ class Case:
             imap, mask = self.m["imap"], self.m["mask"]
             cells = self.batch * int(np.prod(list(self.out_shape)))
             passes = (max(1, int(np.ceil(np.log2(max(cells, 2))))) + 7) // 8
+            # the library takes the bitmap path when the output grid's bitmap fits
+            # the candidates' key space (one bit per cell vs 16 bytes per candidate)
+            bitmap = (cells + 31) // 32 <= 2 * n * K
             if not w.get("inverse"):
-                self.phases.append(Phase("outcoords", outcoords, "build", 16 * n + 16 * n_out + 8,
-                                         kernels="k_candidates, k_radix_*, k_unique_*",
-                                         launches=1 + 3 * passes + 3))
+                self.phases.append(Phase(
+                    "outcoords", outcoords, "build", 16 * n + 16 * n_out + 8,
+                    kernels=("k_bm_mark, k_bm_count, k_scan_exclusive, k_bm_write (bitmap)" if bitmap
+                             else "k_candidates, k_radix_*, k_unique_*"),
+                    launches=4 if bitmap else 1 + 3 * passes + 3))
                 self.phases.append(Phase(
                     "build", lambda: spc.spc_build_indice_map(
                         self.coords, self.batch, self.shape, ksize=self.ks, stride=st, pad=pd,
@@ -494,7 +499,8 @@ def record_traffic(csv_path: str, workload: str, phases):
 
     got = {}
     if "outcoords" in phases:
-        got["outcoords"] = per_call(k(r"k_(candidates|radix|scan|unique)"), r"k_candidates")
+        got["outcoords"] = per_call(k(r"k_(candidates|radix|scan|unique|bm_)"),
+                                    r"k_(candidates|bm_mark)")
     if "build" in phases:
         got["build"] = per_call(k(r"k_(hash_clear|hash_insert|map_probe)"), r"k_map_probe")
     conv = k(r"k_(conv_|gather_gemm)")
@@ -775,7 +781,7 @@ def main():
         if w.get("inverse"):
             phases = ["inverse"]
         if w.get("maxpool"):
-            phases = ["pool", "pool_dgrad"]
+            phases = ["outcoords", "build", "pool", "pool_dgrad"]
         record_traffic(args.record_traffic, args.workload, phases)
         return
     args.warmup = max(args.warmup, 3)
