@@ -73,6 +73,24 @@ def test_subm_small_full(dtype, prec, n, cin, cout):
     assert normwise(to_np(dw), oracle.conv_wgrad(x, dy, imap_ref)) < tol
 
 
+@pytest.mark.parametrize("dtype,cin,cout", [("f32", 16, 16), ("bf16", 64, 64), ("f16", 32, 16)])
+def test_subm_k5(dtype, cin, cout):
+    """5^3 kernel (K = 125, beyond the 32-bit offset masks): forward, mirrored
+    dinput and dfilter (its offset groups of 7 and 8) in full."""
+    g = np.random.default_rng(cin * 7 + cout)
+    batch, shape = 1, (9, 10, 8)
+    coords = rand_coords(g, 400, batch, shape)
+    x, w, b, dy, m, imap_ref = subm_case(coords, batch, shape, cin, cout, dtype, ks=5, seed=cin)
+    d = dev()
+    tol = TOL[(dtype, "exact")]
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], None)
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, imap_ref)) < tol
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, 400)
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, 400)) < tol
+    dw = spc.spc_conv_wgrad(x.to(d), dy.to(d), m["imap"], 125)
+    assert normwise(to_np(dw), oracle.conv_wgrad(x, dy, imap_ref)) < tol
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_k1_gemm_shortcut(dtype):
     g = np.random.default_rng(5)
