@@ -741,20 +741,22 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
                                                    f"rows (map built once, not charged), {t:.1f} s, "
                                                    f"single thread")
     if case_w.get("inverse"):
-        # the inverse conv on the saved maps (not charged): a sample of the
-        # strided output rows scattered back through their pairs
-        n_y = imap.shape[1]
-        y64 = oracle.f64(case_w["y_for"](n_y))
-        per_col = 2.0 * float(cnt.sum()) / max(n_y, 1) * cin * cout
-        cols = int(min(n_y, max(64, budget_s * 1.0e9 / max(per_col, 1.0))))
-        sel = np.linspace(0, n_y - 1, cols).astype(np.int64)
-        sub = np.ascontiguousarray(imap[:, sel])
+        # the inverse conv on the saved maps (not charged): the oracle's forward
+        # gathered through the transposed map (the same sums; the oracle pins
+        # check that identity) on a sample of the output rows
+        oc = oracle.strided_out_coords(c, batch, shape, ks, stride, pad, 1)
+        _, imap_t, cnt = oracle.strided_map(c, oc, batch, shape, ks, stride, pad, 1, True)
+        y64 = oracle.f64(case_w["y_for"](oc.shape[0]))
+        per_row = 2.0 * float(cnt.sum()) / max(n, 1) * cin * cout
+        rows = int(min(n, max(64, budget_s * 1.0e9 / max(per_row, 1.0))))
+        sel = np.linspace(0, n - 1, rows).astype(np.int64)
         t1 = time.perf_counter()
-        oracle.conv_inverse(y64[sel], w64, b64, sub, n)
+        oracle.conv_fwd(y64, w64, b64, imap_t, rows=sel)
         t = time.perf_counter() - t1
-        flops = 2.0 * float((sub >= 0).sum()) * cin * cout
-        return flops / t / 1e12, (f"fp64 inverse conv of {cols} of {n_y} strided output rows "
-                                  f"(maps built once, not charged), {t:.1f} s, single thread")
+        flops = 2.0 * float((imap_t[:, sel] >= 0).sum()) * cin * cout
+        return flops / t / 1e12, (f"fp64 inverse conv (gather through the transposed map) of {rows} "
+                                  f"of {n} output rows (maps built once, not charged), {t:.1f} s, "
+                                  f"single thread")
     n_out = imap.shape[1]
     per_row = 2.0 * float(cnt.sum()) / max(n_out, 1) * cin * cout  # flops per output row
     # rows so that the forward sample takes about the budget at ~1 GFLOP/s
