@@ -131,21 +131,24 @@ spc_status spc_build_indice_map(const int32_t* coords, int64_t n_in, int32_t bat
     t.slots = static_cast<unsigned long long*>(ws);
     t.log2_buckets = ceil_log2((uint64_t)hash_slots_for(n_in)) - 2;
     t.vbits = vbits;
-    // one launch prepares every buffer: zero pair counts, -1 transposed map,
-    // empty table, zero mask, -1 for the mirrored rows of a submanifold map
+    // one launch prepares the table and the pair counts; the insert fills, row
+    // by row, the buffers indexed by input rows: the transposed map (-1), and
+    // for a submanifold map (input rows = output rows) the mirrored map rows
+    // (-1) and the mask (0).  A strided map's mask (output rows) goes here too.
+    const bool mirror = n_out > 0 && probe_mirror(pg, imap_t != nullptr);
     FillList fl;
     int nf = 0;
     fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(pair_count), K, 0u};
-    if (imap_t && n_in > 0) fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(imap_t), (int64_t)K * n_in, 0xFFFFFFFFu};
     if (n_out > 0 || n_in > 0) fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(t.slots), (int64_t)8 << t.log2_buckets, 0xFFFFFFFFu};
-    if (mask && n_out > 0) fl.r[nf++] = FillRegion{mask, n_out, 0u};
-    if (n_out > 0 && probe_mirror(pg, imap_t != nullptr))
-        fl.r[nf++] = FillRegion{reinterpret_cast<uint32_t*>(imap + (int64_t)(pg.centre + 1) * n_out),
-                                (int64_t)(K - pg.centre - 1) * n_out, 0xFFFFFFFFu};
+    if (mask && n_out > 0 && !mirror) fl.r[nf++] = FillRegion{mask, n_out, 0u};
+    RowFill rf{nullptr, 0, 0, nullptr};
+    if (imap_t && n_in > 0) rf = RowFill{imap_t, (int32_t)K, n_in, nullptr};
+    if (mirror) rf = RowFill{imap + (int64_t)(pg.centre + 1) * n_out, (int32_t)(K - pg.centre - 1), n_out, mask};
     spc_status s = build_init(fl, nf, st);
     if (s != SPC_OK) return s;
     if (n_out == 0 && n_in == 0) return SPC_OK;
-    s = hash_insert(coords, n_in, batch, in_shape, t, status, st);
+    if (mirror && n_in == 0) return SPC_OK;
+    s = hash_insert(coords, n_in, batch, in_shape, t, status, rf, st);
     if (s != SPC_OK) return s;
     return map_probe(out_coords, n_out, n_in, pg, t, imap, imap_t, pair_count, mask, status, st);
 }

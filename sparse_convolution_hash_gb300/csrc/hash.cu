@@ -104,12 +104,16 @@ __device__ __forceinline__ void load_bucket(const unsigned long long* slots, uin
 __global__ void __launch_bounds__(kBlock)
 k_hash_insert(const int4* __restrict__ coords, int64_t n, int32_t batch, int D, int H, int W,
               unsigned long long* __restrict__ slots, int log2b, int vbits,
-              int32_t* __restrict__ status)
+              int32_t* __restrict__ status, RowFill fill)
 {
     const uint32_t nb = 1u << log2b, nb_mask = nb - 1;
     const uint32_t bound = 5u * nb + 8u;
     for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n;
          r += (int64_t)gridDim.x * blockDim.x) {
+        // this row's share of the buffers the probe starts from (coalesced
+        // across the warp; hidden behind the insert's round trips)
+        for (int q = 0; q < fill.planes; ++q) fill.p[(int64_t)q * fill.stride + r] = -1;
+        if (fill.mask) fill.mask[r] = 0u;
         const int4 c = coords[r];
         if (c.x < 0 || c.x >= batch || c.y < 0 || c.y >= D || c.z < 0 || c.z >= H || c.w < 0 ||
             c.w >= W) {
@@ -357,13 +361,13 @@ bool probe_mirror(const ProbeGeom& g, bool with_transpose)
 }
 
 spc_status hash_insert(const int32_t* coords, int64_t n, int32_t batch, const int32_t shape[3],
-                       HashTable t, int32_t* status, cudaStream_t st)
+                       HashTable t, int32_t* status, const RowFill& fill, cudaStream_t st)
 {
     if (n == 0) return SPC_OK;
     const int grid = (int)std::min<int64_t>(ceil_div(n, kBlock), 8 * sm_count());
     k_hash_insert<<<grid, kBlock, 0, st>>>(reinterpret_cast<const int4*>(coords), n, batch,
                                            shape[0], shape[1], shape[2], t.slots,
-                                           t.log2_buckets, t.vbits, status);
+                                           t.log2_buckets, t.vbits, status, fill);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }

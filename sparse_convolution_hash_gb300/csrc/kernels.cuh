@@ -51,8 +51,17 @@ struct FillList {
 spc_status build_init(const FillList& L, int n, cudaStream_t st);
 // True when the probe fills a submanifold map through offset mirrors (k <= centre).
 bool probe_mirror(const ProbeGeom& g, bool with_transpose);
+// Per-row fills the insert does for the probe: planes x [stride] int32 set to
+// -1 at each inserted row (the mirrored rows of a submanifold map, or the
+// transposed map), and mask[row] = 0 when mask is given.
+struct RowFill {
+    int32_t* p;
+    int32_t planes;
+    int64_t stride;
+    uint32_t* mask;
+};
 spc_status hash_insert(const int32_t* coords, int64_t n, int32_t batch, const int32_t shape[3],
-                       HashTable t, int32_t* status, cudaStream_t st);
+                       HashTable t, int32_t* status, const RowFill& fill, cudaStream_t st);
 spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const ProbeGeom& g,
                      HashTable t, int32_t* imap, int32_t* imap_t, int32_t* pair_count,
                      uint32_t* mask, int32_t* status, cudaStream_t st);
