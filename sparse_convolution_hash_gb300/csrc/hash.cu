@@ -203,7 +203,7 @@ __device__ __forceinline__ int32_t finish_lookup(const unsigned long long* __res
 // probed; a hit also writes its mirror entry and mirror mask bit, the centre is
 // the identity, and the caller has filled imap rows k > centre with -1 and the
 // mask with 0 beforehand.
-constexpr int kGroup = 3;
+constexpr int kGroup = 2;
 
 // Per-offset table for kernels of at most 32 offsets (precomputed on the host):
 // the cell offset of offset k relative to the query's base cell q*stride - pad,
