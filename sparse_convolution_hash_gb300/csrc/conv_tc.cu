@@ -1,24 +1,26 @@
 // conv_tc.cu -- gathered implicit GEMM on the 5th-generation tensor cores
 // (tcgen05, accumulators in tensor memory) for wide channels.
 //
-// Output-stationary: a CTA owns 256 output rows (two 128-row MMA tiles with
+// Output-stationary: a CTA owns MT x 128 output rows (MT 128-row MMA tiles with
 // their own accumulators, sharing every weight stage) x BN output channels.  It
 // reads its rows' map entries in one burst and skips the offsets no row of the
 // tile uses (rows in a caller's grouped order read their masks first and load
 // only the entries they have).  The K loop then runs over (active offset, 128-byte channel chunk):
-//   warps 0-15 gather the 256 input rows of that offset with 16-byte cp.async
-//     copies straight into a 128-byte-swizzled K-major shared-memory stage (a
-//     warp instruction copies four whole 128-byte row segments; rows with no
-//     neighbour are zero-filled by the copy itself); each thread's copies
-//     arrive on the stage's mbarrier when they land, so no thread waits for
-//     its own data;
-//   one thread of warp 16 loads the BN x 128-byte weight tile with a 2-D TMA
+//   NW gather warps copy the tile's input rows of that offset with 16-byte
+//     cp.async copies straight into a 128-byte-swizzled K-major shared-memory
+//     stage (a warp instruction copies four whole 128-byte row segments; rows
+//     with no neighbour are zero-filled by the copy itself); each thread's
+//     copies arrive on the stage's mbarrier when they land, so no thread waits
+//     for its own data;
+//   one thread of warp NW loads the BN x 128-byte weight tile with a 2-D TMA
 //     load that completes on the same barrier;
-//   one thread of warp 17 waits for the stage, fences the copies into the
-//     async proxy, issues 2 x 4 tcgen05.mma (one per 128-row half, K = 32
+//   one thread of warp NW + 1 waits for the stage, fences the copies into the
+//     async proxy, issues MT x 4 tcgen05.mma (one per 128-row tile, K = 32
 //     bytes each) into the fp32 accumulators in tensor memory, and commits
 //     the stage back to the producers.
-// All offsets accumulate in tensor memory; the epilogue (warps 0-15) reads each
+// Shapes with 8 gather warps run two CTAs per SM, so one CTA's map-entry burst
+// and epilogue overlap the other's gathers.
+// All offsets accumulate in tensor memory; the epilogue (the gather warps) reads each
 // row's accumulators with tcgen05.ld, adds the bias, rounds once and stores the
 // row.  Every output row is written once: no atomics, run-to-run identical.
 //
@@ -78,6 +80,8 @@ struct TcShape {
     static constexpr int B_BYTES = BN * RB;
     static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
     static constexpr int TMEM_COLS = MT * BN <= 32 ? 32 : (MT * BN <= 64 ? 64 : (MT * BN <= 128 ? 128 : (MT * BN <= 256 ? 256 : 512)));
+    // shapes of at most 8 gather warps are built to share an SM with a second CTA
+    static constexpr int kMinCtas = (MT == 1 || NW <= 8) ? 2 : 1;
     static size_t smem_bytes(int K)
     {
         return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
@@ -91,7 +95,7 @@ template <> struct TcKind<__nv_bfloat16> { static constexpr int kind = 0; static
 template <> struct TcKind<float> { static constexpr int kind = 1; static constexpr uint32_t fmt = 2; };
 
 template <typename T, int BN, int STAGES, int MT, int NW, int RB>
-__global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW, RB>::kThreads, (MT == 1 ? 2 : 1))
+__global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW, RB>::kThreads, TcShape<T, BN, STAGES, MT, NW, RB>::kMinCtas)
 k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 {
     using S = TcShape<T, BN, STAGES, MT, NW, RB>;
@@ -452,18 +456,36 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
     return SPC_OK;
 }
 
+// Shared memory of one SM (bytes) and what the runtime reserves per CTA.
+constexpr size_t kSmemPerSm = 233472, kSmemPerCta = 1024;
+
+template <typename T, int BN, int STAGES, int MT, int NW, int RB>
+bool two_per_sm(int K)
+{
+    return 2 * (TcShape<T, BN, STAGES, MT, NW, RB>::smem_bytes(K) + kSmemPerCta) <= kSmemPerSm;
+}
+
 template <typename T>
 spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
 {
-    // one CTA per SM: 2 x 128-row tiles, 16 gather warps, 4 stages (the
-    // fastest of the shapes measured; the gathers are the limiting resource)
     constexpr int E = (int)sizeof(T);
     if (a.cred * E % 128 == 0) {
-        // rows in grouped order run only a few offsets per tile: smaller tiles and
-        // rings let two CTAs share an SM, so one's set-up overlaps the other's work
+        // Two CTAs per SM wherever the tile's shared memory allows: while one
+        // CTA loads its map entries or stores its rows, the other's gathers keep
+        // the SM's copy traffic going.  2 x 128-row tiles with 8 gather warps and
+        // 2 stages fit when the weight stage is 64 wide (any K up to 31) or when K
+        // is small; 128-wide weights with many offsets take 128-row tiles and 3
+        // stages.  One CTA of 2 x 128 rows, 16 warps and 4 stages is the shape
+        // when neither fits.  Rows in grouped order run only a few offsets per
+        // tile and take 128-row tiles.
         if (a.perm && a.n_total % 128 == 0) return launch_tc<T, 128, 2, 1, 8, 128>(a, st);
         if (a.perm) return launch_tc<T, 64, 2, 1, 8, 128>(a, st);
-        if (a.n_total % 128 == 0) return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
+        if (a.n_total % 128 == 0) {
+            if (two_per_sm<T, 128, 2, 2, 8, 128>(a.K)) return launch_tc<T, 128, 2, 2, 8, 128>(a, st);
+            if (two_per_sm<T, 128, 3, 1, 8, 128>(a.K)) return launch_tc<T, 128, 3, 1, 8, 128>(a, st);
+            return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
+        }
+        if (two_per_sm<T, 64, 2, 2, 8, 128>(a.K)) return launch_tc<T, 64, 2, 2, 8, 128>(a, st);
         return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
     }
     // narrow rows (32 or 64 bytes): small stages, many CTAs per SM

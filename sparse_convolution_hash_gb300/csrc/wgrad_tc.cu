@@ -29,7 +29,7 @@ namespace {
 constexpr int kRows = 128;      // reduction rows per stage
 constexpr int kGroup = 8;       // offsets per CTA (one accumulator each)
 constexpr int kStages = 8;      // x-gather stages (a power of two)
-constexpr int kWorkers = 512;   // warps 0-15: gathers; warps 0-3 then run the epilogue
+constexpr int kWorkers = 256;   // warps 0-7: gathers (four 16-byte copies each per stage); warps 0-3 then run the epilogue
 constexpr int kThreads = kWorkers + 64;  // warp 16: dy TMA; warp 17: TMEM owner, MMA issuer
 constexpr int kTmaWarp = kWorkers / 32, kMmaWarp = kTmaWarp + 1;
 constexpr uint64_t kWaitNs = 2000000000ull;

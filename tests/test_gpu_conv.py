@@ -144,6 +144,50 @@ def test_uniform32_strided_bf16():
     assert normwise(to_np(dw), oracle.conv_wgrad(w["x"], dy, imap_ref)) < 2e-2
 
 
+@pytest.mark.parametrize("dtype,cin,cout", [("bf16", 128, 128), ("f16", 64, 128), ("bf16", 128, 64)])
+def test_strided_k2_wide(dtype, cin, cout):
+    """k2 s2 (8 offsets) with wide channels, which selects the tensor-core tile
+    shapes for few offsets (two CTAs of 2 x 128 rows per SM, also with 128-wide
+    weight stages): forward and dinput in full, several tiles and a ragged tail."""
+    g = np.random.default_rng(cin + 3 * cout)
+    batch, shape, n = 2, (24, 22, 26), 3000
+    c = rand_coords(g, n, batch, shape)
+    d = dev()
+    dc = torch.from_numpy(c).to(d)
+    oc, _ = spc.spc_strided_out_coords(dc, batch, shape, 2, 2, 0, 1)
+    m = spc.spc_build_indice_map(dc, batch, shape, ksize=2, stride=2, pad=0, subm=False,
+                                 out_coords=oc, with_transpose=True)
+    spc.check_status(m["status"])
+    oc_ref = oracle.strided_out_coords(c, batch, shape, 2, 2, 0, 1)
+    imap_ref, _, _ = oracle.strided_map(c, oc_ref, batch, shape, 2, 2, 0, 1)
+    assert oc_ref.shape[0] > 4 * 256
+    x = rand_tensor(g, (n, cin), dtype)
+    w = rand_tensor(g, (8, cin, cout), dtype, std=float(np.sqrt(1.0 / (8 * cin))))
+    b = rand_tensor(g, (cout,), dtype, std=0.1)
+    tol = TOL[(dtype, "exact")]
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], m["mask"])
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, imap_ref)) < tol
+    dy = rand_tensor(g, (oc_ref.shape[0], cout), dtype)
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap_t"], spc.SPC_MAP_TRANSPOSED, n)
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, n)) < tol
+
+
+@pytest.mark.parametrize("dtype,cin,cout", [("bf16", 128, 128), ("f16", 128, 64)])
+def test_subm_k1_wide_full(dtype, cin, cout):
+    """1 x 1 x 1 submanifold conv through its (identity) map with wide channels:
+    the one-offset tensor-core tiles, whole output and dinput."""
+    g = np.random.default_rng(cout)
+    batch, shape = 2, (12, 11, 13)
+    coords = rand_coords(g, 1700, batch, shape)
+    x, w, b, dy, m, imap_ref = subm_case(coords, batch, shape, cin, cout, dtype, ks=1, seed=cin)
+    d = dev()
+    tol = TOL[(dtype, "exact")]
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], m["mask"])
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, imap_ref)) < tol
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, 1700)
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, 1700)) < tol
+
+
 @pytest.mark.parametrize("n,cin,cout,dtype,prec", [(777, 16, 16, "f16", "exact"),
                                                   (1000, 128, 128, "bf16", "exact"),
                                                   (3000, 64, 64, "bf16", "exact"),
