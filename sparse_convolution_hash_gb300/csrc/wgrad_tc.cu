@@ -1,7 +1,7 @@
 // wgrad_tc.cu -- dfilter on the tcgen05 tensor cores:
 //   dW[k][c][j] = sum over output rows o with i = imap[k, o] != -1 of x[i][c] dy[o][j].
 //
-// Each CTA owns a group of up to 8 kernel offsets, one 64 x 64 tile of dW
+// Each CTA owns a group of up to 4 kernel offsets, one 64 x 64 tile of dW
 // (input-channel block x output-channel block) and a fixed chunk of output
 // rows.  For every 128-row slice of its chunk it loads the dy rows once (one
 // 2-D TMA load, 128 x 128 bytes) and, for each offset of its group, gathers the
@@ -9,7 +9,8 @@
 // zero-filled, so they add nothing).  The reduction runs over rows, so both
 // operands are MN-major: a gathered row is 64 channels (the M or N index) of
 // one reduction index.  Each offset accumulates into its own 64 x 64 fp32
-// accumulator in tensor memory (8 x 64 columns = all 512).  At the end the
+// accumulator in tensor memory (4 x 64 columns, half of an SM's 512, so two
+// CTAs share an SM and one's waits overlap the other's gathers).  At the end the
 // CTA writes its partial tiles to the workspace; k_wgrad_reduce sums the
 // chunks in a fixed order, so dW is run-to-run bit-identical.
 //
@@ -27,8 +28,8 @@ namespace spc {
 namespace {
 
 constexpr int kRows = 128;      // reduction rows per stage
-constexpr int kGroup = 8;       // offsets per CTA (one accumulator each)
-constexpr int kStages = 8;      // x-gather stages (a power of two)
+constexpr int kGroup = 4;       // offsets per CTA (one accumulator each)
+constexpr int kStages = 4;      // x-gather stages (a power of two)
 constexpr int kWorkers = 256;   // warps 0-7: gathers (four 16-byte copies each per stage); warps 0-3 then run the epilogue
 constexpr int kThreads = kWorkers + 64;  // warp 16: dy TMA; warp 17: TMEM owner, MMA issuer
 constexpr int kTmaWarp = kWorkers / 32, kMmaWarp = kTmaWarp + 1;
@@ -40,11 +41,11 @@ template <typename T> struct TcKindW;
 template <> struct TcKindW<__half> { static constexpr uint32_t fmt = 0; };
 template <> struct TcKindW<__nv_bfloat16> { static constexpr uint32_t fmt = 1; };
 
-// At least 120 KB, so that one CTA (which takes all 512 TMEM columns) owns its SM.
+// About 97 KB: two CTAs fit in an SM's shared memory (and its tensor memory).
 size_t smem_bytes()
 {
     const size_t need = 1024 + (size_t)kStages * kABytes + 2 * (size_t)kBBytes + 8 * (2 * kStages + 5) + 64;
-    return need > 120 * 1024 ? need : 120 * 1024;
+    return need;
 }
 
 // MN-major operand, 128-byte swizzle: 8 reduction rows of 128 bytes per atom,
@@ -61,7 +62,7 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr)
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -85,7 +86,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     const int ct = t % tiles_c;
     const int kg = t / tiles_c;
     // the K offsets are split into ceil(K / kGroup) groups of near-equal size
-    // (27 -> 7, 7, 7, 6), so every CTA of a row split does the same work
+    // (27 -> 4, 4, 4, 4, 4, 4, 3), so every CTA of a row split does about the same work
     const int n_groups = (a.K + kGroup - 1) / kGroup;
     const int g_base = a.K / n_groups, g_rem = a.K % n_groups;
     const int k0 = kg * g_base + (kg < g_rem ? kg : g_rem);
@@ -112,7 +113,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     }
     if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tma_dy);
     if (warp == kMmaWarp) {
-        ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[1]), 512);
+        ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[1]), kGroup * 64);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -267,7 +268,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     __syncthreads();
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 512);
+        ptx::tmem_dealloc(tmem, kGroup * 64);
     }
 }
 
@@ -326,13 +327,13 @@ bool wgrad_tc_supported(int32_t K, int32_t cin, int32_t cout, spc_dtype dt)
     return (dt == SPC_F16 || dt == SPC_BF16) && K >= 1 && cin % 64 == 0 && cout % 64 == 0;
 }
 
-// Row splits: at most one CTA per SM of a 152-SM GB300 (a CTA takes all of its
-// SM's tensor memory, so one more CTA than SMs would double the time).  A fixed
-// target (not the device's SM count) keeps the summation order, and so the
-// result bits, the same on every device.
+// Row splits: at most two CTAs per SM of a 152-SM GB300 (a CTA takes half of its
+// SM's tensor memory, so more CTAs than that would wait for a second wave).  A
+// fixed target (not the device's SM count) keeps the summation order, and so
+// the result bits, the same on every device.
 int wgrad_tc_splits(int32_t K, int64_t n_out, int32_t cin, int32_t cout)
 {
-    constexpr int64_t kTargetCtas = 152;
+    constexpr int64_t kTargetCtas = 304;
     const int64_t tiles = (int64_t)((K + kGroup - 1) / kGroup) * (cin / 64) * (cout / 64);
     int64_t s = tiles > 0 ? kTargetCtas / tiles : 1;
     const int64_t max_s = n_out > 0 ? (n_out + kRows - 1) / kRows : 1;

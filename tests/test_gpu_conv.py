@@ -76,7 +76,7 @@ def test_subm_small_full(dtype, prec, n, cin, cout):
 @pytest.mark.parametrize("dtype,cin,cout", [("f32", 16, 16), ("bf16", 64, 64), ("f16", 32, 16)])
 def test_subm_k5(dtype, cin, cout):
     """5^3 kernel (K = 125, beyond the 32-bit offset masks): forward, mirrored
-    dinput and dfilter (its offset groups of 7 and 8) in full."""
+    dinput and dfilter (its offset groups of 3 and 4) in full."""
     g = np.random.default_rng(cin * 7 + cout)
     batch, shape = 1, (9, 10, 8)
     coords = rand_coords(g, 400, batch, shape)
