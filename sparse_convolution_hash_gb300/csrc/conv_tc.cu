@@ -21,8 +21,11 @@
 // Shapes with 8 gather warps run two CTAs per SM, so one CTA's map-entry burst
 // and epilogue overlap the other's gathers.
 // All offsets accumulate in tensor memory; the epilogue (the gather warps) reads each
-// row's accumulators with tcgen05.ld, adds the bias, rounds once and stores the
-// row.  Every output row is written once: no atomics, run-to-run identical.
+// row's accumulators with tcgen05.ld, adds the bias, rounds once and, for rows in
+// tile order, stages the tile in the freed stage buffers as 128-byte-swizzled
+// boxes that one thread stores with 2-D TMA (rows in a caller's order are
+// stored by their threads).  Every output row is written once: no atomics,
+// run-to-run identical.
 //
 // Forward: B = the weight slice transposed to [Cout][Cin] (K-major), prepared
 // once per call in the workspace.  dinput: rows are input rows, the map is the
@@ -82,6 +85,10 @@ struct TcShape {
     static constexpr int TMEM_COLS = MT * BN <= 32 ? 32 : (MT * BN <= 64 ? 64 : (MT * BN <= 128 ? 128 : (MT * BN <= 256 ? 256 : 512)));
     // shapes of at most 8 gather warps are built to share an SM with a second CTA
     static constexpr int kMinCtas = (MT == 1 || NW <= 8) ? 2 : 1;
+    // The epilogue can stage the tile's output (rows x BN) in the freed stage
+    // buffers as 128-row x 128-byte boxes and store them with TMA.
+    static constexpr bool kTmaStore =
+        (BN * ELEM) % 128 == 0 && (size_t)kRowsPerCta * BN * ELEM <= (size_t)STAGES * STAGE_BYTES;
     static size_t smem_bytes(int K)
     {
         return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
@@ -96,7 +103,8 @@ template <> struct TcKind<float> { static constexpr int kind = 1; static constex
 
 template <typename T, int BN, int STAGES, int MT, int NW, int RB>
 __global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW, RB>::kThreads, TcShape<T, BN, STAGES, MT, NW, RB>::kMinCtas)
-k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
+k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ CUtensorMap tma_o,
+          int tstore)
 {
     using S = TcShape<T, BN, STAGES, MT, NW, RB>;
     constexpr int kRowsPerCta = S::kRowsPerCta, kWorkers = S::kWorkers;
@@ -337,30 +345,60 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b)
 #pragma unroll
                     for (int j = 0; j < kCols; ++j) v[j] = 0u;
                 }
-                if (evalid) {
-                    T* dst = out + erow * a.n_total + n0 + c;
-                    constexpr int kVec = (int)(kCols * sizeof(T) / 16);  // 16-byte words per chunk
-                    alignas(16) T rsd[kCols];
-                    if (a.residual) {
-                        const uint4* r4 = reinterpret_cast<const uint4*>(
-                            static_cast<const T*>(a.residual) + erow * a.n_total + n0 + c);
+                constexpr int kVec = (int)(kCols * sizeof(T) / 16);  // 16-byte words per chunk
+                const bool use_res = a.residual && evalid;
+                alignas(16) T rsd[kCols];
+                if (use_res) {
+                    const uint4* r4 = reinterpret_cast<const uint4*>(
+                        static_cast<const T*>(a.residual) + erow * a.n_total + n0 + c);
 #pragma unroll
-                        for (int q = 0; q < kVec; ++q) reinterpret_cast<uint4*>(rsd)[q] = __ldcs(r4 + q);
-                    }
-                    alignas(16) T o[kCols];
-#pragma unroll
-                    for (int j = 0; j < kCols; ++j) {
-                        float f = __uint_as_float(v[j]);
-                        if (bias) f += elem<T>::to_f32(bias[n0 + c + j]);
-                        if (a.residual) f = fmaf(a.add_scale, elem<T>::to_f32(rsd[j]), f);
-                        if (a.act) f = fmaxf(f, 0.f);
-                        o[j] = elem<T>::from_f32(f);
-                    }
-                    const uint4* o4 = reinterpret_cast<const uint4*>(o);
-                    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-                    for (int q = 0; q < (int)(kCols * sizeof(T) / 16); ++q) __stcs(d4 + q, o4[q]);  // streamed out
+                    for (int q = 0; q < kVec; ++q) reinterpret_cast<uint4*>(rsd)[q] = __ldcs(r4 + q);
                 }
+                alignas(16) T o[kCols];
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) {
+                    float f = __uint_as_float(v[j]);
+                    if (bias) f += elem<T>::to_f32(bias[n0 + c + j]);
+                    if (use_res) f = fmaf(a.add_scale, elem<T>::to_f32(rsd[j]), f);
+                    if (a.act) f = fmaxf(f, 0.f);
+                    o[j] = elem<T>::from_f32(f);
+                }
+                const uint4* o4 = reinterpret_cast<const uint4*>(o);
+                if (S::kTmaStore && tstore) {
+                    // into box (half, c / kBoxCols): row r at 128 r, its 16-byte
+                    // pieces swizzled by r % 8 as the TMA store reads them
+                    constexpr int kBoxCols = 128 / (int)sizeof(T);
+                    const int r = quarter * 32 + lane;
+                    uint8_t* box = smem + (size_t)(half * (BN / kBoxCols) + c / kBoxCols) * (kHalf * 128);
+                    const int j0 = (c % kBoxCols) * (int)sizeof(T) / 16;
+#pragma unroll
+                    for (int q = 0; q < kVec; ++q)
+                        *reinterpret_cast<uint4*>(box + r * 128 + (((j0 + q) ^ (r & 7)) << 4)) = o4[q];
+                } else if (evalid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(out + erow * a.n_total + n0 + c);
+#pragma unroll
+                    for (int q = 0; q < kVec; ++q) __stcs(d4 + q, o4[q]);  // streamed out
+                }
+            }
+        }
+        if (S::kTmaStore && tstore) {
+            // every epilogue thread reaches this barrier (aborted or not); the
+            // staged boxes leave once all rows are in place
+            if (aborted && lane == 0) atomicExch(&s_ctrl[1], 1);
+            ptx::fence_proxy_async_smem();
+            ptx::bar_sync_named(1, kWorkers);
+            if (tid == 0 && s_ctrl[1] == 0) {
+                constexpr int kBoxCols = 128 / (int)sizeof(T);
+                for (int h = 0; h < MT; ++h) {
+                    const int64_t y = row0 + h * kHalf;
+                    if (y >= a.rows) break;  // rows past the end inside a box are clipped
+#pragma unroll
+                    for (int bx = 0; bx < BN / kBoxCols; ++bx)
+                        ptx::tma_store2d(&tma_o, n0 + bx * kBoxCols, (int32_t)y,
+                                         ptx::smem_u32(smem + (size_t)(h * (BN / kBoxCols) + bx) * (kHalf * 128)));
+                }
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();  // shared memory must outlive the stores' reads
             }
         }
     }
@@ -439,6 +477,17 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
     CUtensorMap tb;
     if (!make_tmap<T, RB>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN))
         return SPC_ERR_UNSUPPORTED;
+    // Output rows in tile order (no caller permutation) leave through TMA stores
+    // when the output is a valid tensor-map target (16-byte aligned base).
+    CUtensorMap to = tb;
+    int tstore = 0;
+    if (S::kTmaStore && a.perm == nullptr) {
+        CUtensorMap m;
+        if (make_tmap<T, 128>(&m, a.out, (uint64_t)a.n_total, (uint64_t)a.rows, kHalf)) {
+            to = m;
+            tstore = 1;
+        }
+    }
     const size_t smem = S::smem_bytes(a.K);
     auto kern = k_conv_tc<T, BN, STAGES, MT, NW, RB>;
     static bool configured[64] = {};
@@ -451,7 +500,7 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
         configured[dev] = true;
     }
     dim3 grid((unsigned)ceil_div(a.rows, S::kRowsPerCta), (unsigned)(a.n_total / BN));
-    kern<<<grid, S::kThreads, smem, st>>>(a, tb);
+    kern<<<grid, S::kThreads, smem, st>>>(a, tb, to, tstore);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }

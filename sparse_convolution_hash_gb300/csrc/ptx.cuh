@@ -32,6 +32,13 @@ __device__ __forceinline__ void mbar_init_fence()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Named barrier `id` (1..15) over `threads` threads (a multiple of 32); orders
+// the participants' shared-memory accesses like __syncthreads.
+__device__ __forceinline__ void bar_sync_named(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
@@ -102,6 +109,25 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
 }
 
 // One box of a 2-D tensor at (x, y).
+// 2-D TMA store of one box from shared memory, tracked as a bulk group.
+__device__ __forceinline__ void tma_store2d(const void* tmap, int32_t x, int32_t y, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Returns once every committed bulk group has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_tile2d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                            uint64_t* bar)
 {
