@@ -498,14 +498,20 @@ class Case:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: traffic figures taken from other sources are void."""
+    """Hash of the CUDA sources' code (comments and blank space removed):
+    traffic figures taken from other code are void, a comment edit is not."""
     import glob
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "sparse_convolution_hash_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)  # block comments
+        code = re.sub(r"//[^\n]*", " ", code)                # line comments (no string here holds //)
+        code = " ".join(code.split())
+        h.update(os.path.basename(f).encode() + b"\0" + code.encode() + b"\0")
     return h.hexdigest()[:16]
 
 

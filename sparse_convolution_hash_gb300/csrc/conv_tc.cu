@@ -229,11 +229,12 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
     const uint8_t* in = static_cast<const uint8_t*>(a.in);
     if (tid < kWorkers) {
         // -------------------------------------------------- row-gather producers
-        // A stage: 256 rows x 8 chunks of 16 bytes; chunk e = j * 512 + tid, so a
-        // warp instruction copies four whole 128-byte row segments.  Sixteen
-        // warps keep enough copies in flight to cover L2 latency.  Each
-        // thread's copies arrive on the stage's barrier when they complete, so
-        // the thread never waits for its own data, only for a free stage.
+        // A stage: the tile's rows x RB / 16 chunks of 16 bytes; chunk e = j *
+        // kWorkers + tid, so a warp instruction copies whole row segments (four
+        // of 128 bytes).  The gather warps of the SM's CTAs (16 per SM) keep
+        // enough copies in flight to cover L2 latency.  Each thread's copies
+        // arrive on the stage's barrier when they complete, so the thread never
+        // waits for its own data, only for a free stage.
         // feature rows are re-read by up to K output rows: keep them in L2
         const uint64_t keep = ptx::policy_evict_last();
         for (int it = 0; it < n_iter; ++it) {
