@@ -1,15 +1,18 @@
 """Benchmark of the sparse-convolution hot path on one or more GPUs.
 
-Default workload (one JSON line): the LiDAR-like scene, batch 2, 41 x 1600 x
-1408 grid, 120,000 voxels, fp16 features 16 -> 16.  One step = one pass of
-its hot path: spc_build_indice_map (validate + key + hash build + probe of all
-27 offsets) then spc_conv_fwd over the map.  The headline value is conv
-TFLOP/s over active pairs (2 * P * Cin * Cout per step) over the whole step
-time; the indice-map rate (Mvoxel/s) and per-phase times are reported beside
-it.  Other workloads (--workload) cover the remaining rows of the path: the
+Default workload (one JSON line): the training step of a 64 -> 64 bf16
+submanifold layer on four 192^3 surface shells (498,145 voxels, batch index in
+coordinate column 0).  One step = one pass of its hot path:
+spc_build_indice_map (validate + key + hash build + probe of all 27 offsets),
+spc_conv_fwd, spc_conv_dgrad (dinput through the mirrored map) and
+spc_conv_wgrad (dfilter, fp32).  The headline value is conv TFLOP/s over
+active pairs (2 * P * Cin * Cout per conv pass, three passes) over the whole
+step time; the indice-map rate (Mvoxel/s) and per-phase times are reported
+beside it.  Other workloads (--workload) cover the remaining rows of the
+path: the LiDAR-like scene (batch 2, 41 x 1600 x 1408, fp16 16 -> 16), the
 strided k3 s2 p1 conv (output coordinates + maps + forward), the 256^3 shell
-at 128 -> 128 (k3 and k1), and the 4 x 192^3 training step (forward, dinput,
-dfilter).
+at 128 -> 128 (k3 and k1), and the inverse conv, fused residual block and max
+pool built on the same maps.
 
 Timing: every phase is captured once as a CUDA graph (the C ABI allocates
 nothing and only enqueues on the current stream) and replayed; CUDA events on
@@ -48,7 +51,7 @@ sys.path.insert(0, ROOT)
 import scenes  # noqa: E402
 
 METRIC = "SubM3d conv TFLOP/s over active pairs (and % roofline); indice-map Mvoxel/s"
-DEFAULT_WORKLOAD = "lidar_subm_f16"
+DEFAULT_WORKLOAD = "shell192x4_train_bf16"
 L2_FLUSH_BYTES = 256 << 20
 SHAPES = {"uniform32": (32, 32, 32), "lidar": (41, 1600, 1408), "shell256": (256, 256, 256),
           "shell192x4": (192, 192, 192)}
@@ -538,7 +541,7 @@ def record_traffic(csv_path: str, workload: str, phases):
     into profiles/dram_traffic.json, keyed by the current kernel-source hash.
 
     Kernels are grouped by phase: out-coords (candidates, radix sort, unique),
-    build (table clear, insert, map probe), conv (weight transpose + gather
+    build (table and count init, insert, map probe), conv (weight transpose + gather
     kernels; with a backward pass the conv launches alternate forward, dinput)
     and dfilter.  A phase's bytes are its kernels' bytes divided by the number
     of its calls (counted by one anchor kernel per phase)."""
@@ -570,7 +573,7 @@ def record_traffic(csv_path: str, workload: str, phases):
         got["outcoords"] = per_call(k(r"k_(candidates|radix|scan|unique|bm_)"),
                                     r"k_(candidates|bm_mark)")
     if "build" in phases:
-        got["build"] = per_call(k(r"k_(hash_clear|hash_insert|map_probe)"), r"k_map_probe")
+        got["build"] = per_call(k(r"k_(build_init|hash_insert|map_probe)"), r"k_map_probe")
     conv = k(r"k_(conv_|gather_gemm)")
     fwd, dgr = (conv[0::2], conv[1::2]) if "dgrad" in phases else (conv, [])
     tr = k(r"k_transpose_w")

@@ -159,10 +159,13 @@ SPC_API spc_status spc_build_indice_map(const int32_t* coords, int64_t n_in, int
  *  which every GPU that loads the library keeps until the process exits.
  *  n_in may be at most SPC_NOALLOC_MAX_VOXELS; larger inputs return
  *  SPC_ERR_WORKSPACE before any work is enqueued.
- *  The first call on a device looks up the array's device address (once per
- *  device, with that device current); make that first call before any stream
- *  capture.  The call allocates nothing and synchronises nothing.
- *  All calls on a device share the one table.  Each call clears it before use,
+ *  The first call in a CUDA context looks up the array's device address in
+ *  that context (with the caller's device current) and caches it by the
+ *  context's unique id; after cudaDeviceReset or in another context the
+ *  array sits at another address, and the next call there looks it up again.
+ *  Make the first call in a context before any stream capture.  The call
+ *  allocates nothing and synchronises nothing.
+ *  All calls in a context share the one table.  Each call clears it before use,
  *  but calls whose GPU work overlaps (other streams, other host threads) race
  *  on it: the caller must serialise them. */
 #define SPC_NOALLOC_MAX_VOXELS 1048576

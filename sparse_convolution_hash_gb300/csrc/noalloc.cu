@@ -6,15 +6,22 @@
 // 64-bit slots (16 MiB).  Every device that loads this library holds that
 // array until the process exits.  In host code the array's name is only a
 // host-side stand-in, never a device address, so the entry point looks the
-// real address up once per device with cudaGetSymbolAddress (with that device
-// current) and hands that pointer to the kernels as their workspace.
+// real address up with cudaGetSymbolAddress (with the caller's device current)
+// and hands that pointer to the kernels as their workspace.
 //
-// All calls on a device share the one table.  Each call clears it before use,
+// The address belongs to the CUDA context the module was loaded into, not to
+// the device number: after cudaDeviceReset, or in another context on the same
+// device, the module is loaded again at another address.  The cache is
+// therefore keyed by the unique id of the current context (cuCtxGetCurrent and
+// cuCtxGetId, reached through the runtime's driver entry points so that nothing
+// links libcuda), and a call in a context it has not seen looks the address up
+// again.
+//
+// All calls in a context share the one table.  Each call clears it before use,
 // so no state carries from one call to the next, but calls whose work overlaps
 // on the GPU (different streams, or different host threads) race on it and
 // must be serialised by the caller.
-#include <mutex>
-
+#include "ctx_cache.h"
 #include "kernels.cuh"
 
 namespace {
@@ -24,27 +31,54 @@ constexpr int64_t kSlots = 2 * kMaxVoxels;  // load factor <= 1/2, as for the wo
 
 static __device__ __align__(256) unsigned long long g_noalloc_table[kSlots];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void* g_table_addr[kMaxDevices] = {nullptr};
+typedef int (*CtxGetCurrentFn)(void**);
+typedef int (*CtxGetIdFn)(void*, unsigned long long*);
 
-// Device address of the table on the current device (looked up once per device).
-spc_status table_address(void** out)
+template <typename Fn>
+Fn driver_fn(const char* name)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SPC_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return SPC_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_table_addr[dev]) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint(name, &p, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the current context; false when there is none.
+bool current_ctx_id(unsigned long long* id)
+{
+    static CtxGetCurrentFn get = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    void* ctx = nullptr;
+    return get && get_id && get(&ctx) == 0 && ctx && get_id(ctx, id) == 0;
+}
+
+spc::CtxCache<16> g_cache;
+
+bool lookup(void** p) { return cudaGetSymbolAddress(p, g_noalloc_table) == cudaSuccess; }
+
+}  // namespace
+
+namespace spc {
+
+// Device address of the table in the caller's current context.
+spc_status noalloc_table_address(void** out)
+{
+    unsigned long long id = 0;
+    if (!current_ctx_id(&id)) {
+        // no current context yet: the runtime makes the device's primary
+        // context current on its first call that needs one
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_table) != cudaSuccess || !p) return SPC_ERR_CUDA;
-        g_table_addr[dev] = p;
+        if (!lookup(&p) || !p || !current_ctx_id(&id)) return SPC_ERR_CUDA;
     }
-    *out = g_table_addr[dev];
+    void* p = g_cache.get(id, lookup);
+    if (!p) return SPC_ERR_CUDA;
+    *out = p;
     return SPC_OK;
 }
 
-}  // namespace
+}  // namespace spc
 
 extern "C" SPC_API spc_status spc_build_indice_map_noalloc(
     const int32_t* coords, int64_t n_in, int32_t batch, const int32_t in_shape[3],
@@ -56,7 +90,7 @@ extern "C" SPC_API spc_status spc_build_indice_map_noalloc(
     const size_t need = spc_indice_map_workspace_size(n_in);
     if (need > sizeof(unsigned long long) * (size_t)kSlots) return SPC_ERR_WORKSPACE;
     void* table = nullptr;
-    const spc_status s = table_address(&table);
+    const spc_status s = spc::noalloc_table_address(&table);
     if (s != SPC_OK) return s;
     return spc_build_indice_map(coords, n_in, batch, in_shape, g, subm, out_coords, n_out, imap,
                                 imap_t, pair_count, mask, status, table,

@@ -95,20 +95,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // ---------------------------------------------------------------- TMA
-// Four rows (row coordinates r0..r3, each one box row high) of a 2-D tensor
-// starting at column x, written to consecutive 128-byte rows at dst with the
-// tensor map's swizzle; out-of-range rows are filled with zeros.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// One box of a 2-D tensor at (x, y).
 // 2-D TMA store of one box from shared memory, tracked as a bulk group.
 __device__ __forceinline__ void tma_store2d(const void* tmap, int32_t x, int32_t y, uint32_t src)
 {

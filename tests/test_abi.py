@@ -189,3 +189,16 @@ def test_binding_refuses_without_library(monkeypatch):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(binding.SpcLibraryMissing):
         binding.lib()
+
+
+def test_noalloc_context_cache_logic(tmp_path):
+    """The allocation-free build caches its table's device address per CUDA
+    context id; compiled and run on the host with the library's own header."""
+    exe = tmp_path / "ctx_cache_check"
+    src = os.path.join(ROOT, "tests", "ctx_cache_check.cpp")
+    inc = os.path.join(ROOT, "sparse_convolution_hash_gb300", "csrc")
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", inc, src, "-o", str(exe), "-lpthread"],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "ctx cache ok" in out.stdout
