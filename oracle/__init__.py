@@ -42,7 +42,8 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC])
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -92,6 +93,11 @@ def _load():
             lib.orc_conv_wgrad_entries.argtypes = [_F64P, _F64P, _I32P, _i64, _i64, _i64, _i32,
                                                    _i32, _I64P, _i64, _F64P]
             lib.orc_conv_wgrad_entries.restype = None
+            _I8P = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+            _F32P = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+            lib.orc_conv_fwd_int8.argtypes = [_I8P, _I8P, _F32P, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_float, _i32, ctypes.c_void_p, _i64, _i64,
+                                              _i64, _i32, _i32, _I8P, _I32P]
             _lib = lib
     return _lib
 
@@ -303,3 +309,41 @@ def conv_wgrad_entries(x, dy, imap, entries):
     v = np.empty(e.shape[0], dtype=np.float64)
     lib.orc_conv_wgrad_entries(x, dy, m, K, n_in, n_out, cin, cout, e, e.shape[0], v)
     return v
+
+
+def _np(t, dtype):
+    if hasattr(t, "detach"):
+        t = t.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(t), dtype=dtype)
+
+
+def conv_fwd_int8(x, w, scale, bias, imap, add=None, add_scale=0.0, relu=False):
+    """Quantized forward (spconv's int8 implicit GEMM rule): int8 codes x [N_in, Cin]
+    and w [K, Cin, Cout], fp32 per-channel scale [Cout] and bias [Cout] (or None),
+    optional int8 residual add [N_out, Cout] with an fp32 scale, optional ReLU.
+    imap [K, N_out], or None for K = 1 on the identity map.  Returns (y int8
+    [N_out, Cout], acc int32 [N_out, Cout] -- the exact integer sums)."""
+    lib = _load()
+    xq, wq = _np(x, np.int8), _np(w, np.int8)
+    K, cin, cout = wq.shape
+    n_in = xq.shape[0]
+    assert xq.shape[1] == cin
+    if imap is None:
+        assert K == 1
+        m, n_out = None, n_in
+    else:
+        m = np.ascontiguousarray(imap, dtype=np.int32)
+        assert m.shape[0] == K
+        n_out = m.shape[1]
+    sc = _np(scale, np.float32)
+    b = _np(bias, np.float32) if bias is not None else None
+    a = _np(add, np.int8) if add is not None else None
+    y = np.empty((n_out, cout), dtype=np.int8)
+    acc = np.empty((n_out, cout), dtype=np.int32)
+    st = lib.orc_conv_fwd_int8(xq, wq, sc, b.ctypes.data if b is not None else None,
+                               a.ctypes.data if a is not None else None, float(add_scale),
+                               1 if relu else 0, m.ctypes.data if m is not None else None, K, n_in,
+                               n_out, cin, cout, y, acc)
+    if st != OK:
+        raise OracleError(st, "conv_fwd_int8")
+    return y, acc

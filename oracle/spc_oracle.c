@@ -37,6 +37,7 @@
  *
  * All floating point is double precision on the exact input values.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -478,4 +479,69 @@ void orc_conv_wgrad_entries(const double* x, const double* dy, const int32_t* im
         }
         vals[e] = s;
     }
+}
+
+/*
+ * Quantized forward: spconv's int8 implicit GEMM with per-output-channel scale
+ * and bias (spconv docs, TENSORRT_INT8_GUIDE.md: "Spconv Int8 Scale/Bias
+ * Conversion Basic Rule", "Call Spconv Implicit GEMM with Calculated Scales and
+ * Bias", "Calculate Spconv Int8 Scale and Bias from PyTorch Quantized Layer").
+ * Values are int8 codes; a code q stands for q * its scale, and a real value v
+ * is stored as saturate(round(v / scale)).  With
+ *   scale[j] = input_scale * weight_scale[j] / output_scale,
+ *   bias[j]  = bias_fp[j] / output_scale,
+ * the output code of row o, channel j is
+ *   acc = sum over pairs (k, i = imap[k, o] != -1) of sum_c x[i, c] w[k, c, j]
+ *         (exact integer sum, kept in 32 bits as the integer GEMM does),
+ *   f   = float(acc) * scale[j] + bias[j],
+ *   f   = f + add_scale * float(add[o, j])   (fused residual add, when given),
+ *   f   = max(f, 0)                          (ReLU, when asked),
+ *   y   = saturate(round(f)) to [-128, 127], round half away from zero
+ *         (C's round, the plain reading of the rule's round()).
+ * Every floating-point operation is an fp32 operation rounded once, in the
+ * order written (the rule's data are fp32); nothing is fused.  acc_out
+ * (nullable) receives the integer sums.  Returns ORC_ERR_ARG if a sum leaves
+ * the 32-bit range.
+ */
+int orc_conv_fwd_int8(const int8_t* x, const int8_t* w, const float* scale, const float* bias,
+                      const int8_t* add, float add_scale, int32_t relu, const int32_t* imap,
+                      int64_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout, int8_t* y,
+                      int32_t* acc_out)
+{
+    (void)n_in;
+    int64_t* acc = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cout > 0 ? cout : 1));
+    if (!acc) return ORC_ERR_NOMEM;
+    for (int64_t o = 0; o < n_out; ++o) {
+        for (int32_t j = 0; j < cout; ++j) acc[j] = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            int32_t i = imap ? imap[k * n_out + o] : (int32_t)o;
+            if (i < 0) continue;
+            const int8_t* xi = x + (int64_t)i * cin;
+            const int8_t* wk = w + k * cin * cout;
+            for (int32_t c = 0; c < cin; ++c)
+                for (int32_t j = 0; j < cout; ++j)
+                    acc[j] += (int64_t)xi[c] * (int64_t)wk[(int64_t)c * cout + j];
+        }
+        for (int32_t j = 0; j < cout; ++j) {
+            if (acc[j] > INT32_MAX || acc[j] < INT32_MIN) {
+                free(acc);
+                return ORC_ERR_ARG;
+            }
+            if (acc_out) acc_out[o * cout + j] = (int32_t)acc[j];
+            float f = (float)(int32_t)acc[j];
+            f = f * scale[j];
+            if (bias) f = f + bias[j];
+            if (add) {
+                float t = add_scale * (float)add[o * cout + j];
+                f = f + t;
+            }
+            if (relu && f < 0.0f) f = 0.0f;
+            float r = roundf(f);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -128.0f) r = -128.0f;
+            y[o * cout + j] = (int8_t)r;
+        }
+    }
+    free(acc);
+    return ORC_OK;
 }

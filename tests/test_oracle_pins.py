@@ -476,3 +476,96 @@ def test_sampled_helpers_match_full():
     np.testing.assert_allclose(oracle.conv_wgrad_entries(x, dy, imap, ent),
                                oracle.conv_wgrad(x, dy, imap).reshape(-1)[ent], rtol=1e-13,
                                atol=1e-13)
+
+
+# ------------------------------------------------------------------ int8 rule
+
+def test_int8_golden_two_voxels():
+    """Hand-worked cases of the int8 rule (rounding ties, ReLU, saturation, the
+    residual add) on a two-voxel scene: tests/golden/int8_two_voxel_rule.txt."""
+    c = np.array([[0, 0, 0, 0], [0, 0, 0, 1]], dtype=np.int32)
+    imap, _ = oracle.subm_map(c, 1, (4, 4, 4))
+    x = np.array([[3], [-5]], dtype=np.int8)
+    w = np.zeros((27, 1, 1), dtype=np.int8)
+    w[13], w[14], w[12] = 2, 7, -1
+    rows = 0
+    for line in open(os.path.join(GOLDEN, "int8_two_voxel_rule.txt")):
+        line = line.split("#")[0].split()
+        if not line:
+            continue
+        sc, b, a0, a1, asc, relu, y0, y1 = line
+        add = None if a0 == "none" else np.array([[int(a0)], [int(a1)]], dtype=np.int8)
+        y, acc = oracle.conv_fwd_int8(x, w, np.array([float(sc)], np.float32),
+                                      np.array([float(b)], np.float32), imap, add=add,
+                                      add_scale=float(asc), relu=relu == "1")
+        assert acc.ravel().tolist() == [-29, -13]
+        assert y.ravel().tolist() == [int(y0), int(y1)], line
+        rows += 1
+    assert rows == 6
+
+
+def _int8_case(seed, n=300, batch=2, shape=(7, 8, 9), cin=24, cout=20):
+    g = np.random.default_rng(seed)
+    coords = rand_coords(g, n, batch, shape)
+    imap, _ = oracle.subm_map(coords, batch, shape)
+    x = g.integers(-128, 128, size=(n, cin)).astype(np.int8)
+    w = g.integers(-128, 128, size=(27, cin, cout)).astype(np.int8)
+    return coords, imap, x, w, g
+
+
+def test_int8_sums_equal_the_fp64_forward():
+    """The integer sums are the pinned float forward of the same integer values
+    (every partial sum is an integer far below 2^53, so fp64 is exact)."""
+    _, imap, x, w, _ = _int8_case(11)
+    _, acc = oracle.conv_fwd_int8(x, w, np.ones(w.shape[2], np.float32), None, imap)
+    ref = oracle.conv_fwd(x.astype(np.float64), w.astype(np.float64), None, imap)
+    assert np.array_equal(acc.astype(np.float64), ref)
+
+
+def test_int8_k1_is_integer_gemm():
+    g = np.random.default_rng(12)
+    x = g.integers(-128, 128, size=(50, 16)).astype(np.int8)
+    w = g.integers(-128, 128, size=(1, 16, 8)).astype(np.int8)
+    _, acc = oracle.conv_fwd_int8(x, w, np.ones(8, np.float32), None, None)
+    assert np.array_equal(acc, x.astype(np.int64) @ w[0].astype(np.int64))
+
+
+def test_int8_scales_reproduce_the_dequantized_float_conv():
+    """scale = input_scale * weight_scale[j] / output_scale and bias / output_scale
+    (the page's conversion from a quantized layer) make the code the quantized
+    float conv of the dequantized tensors: equal codes except within fp32
+    rounding of a rounding tie, and never more than one code apart."""
+    _, imap, x, w, g = _int8_case(13, cin=16, cout=12)
+    w = (w // 8).astype(np.int8)  # keep outputs mostly inside the int8 range
+    s_in = np.float32(0.05)
+    s_w = g.uniform(0.002, 0.02, size=w.shape[2]).astype(np.float32)
+    s_out = np.float32(0.09)
+    bias_fp = g.normal(0, 0.5, size=w.shape[2])
+    scale = (s_in * s_w / s_out).astype(np.float32)
+    bias = (bias_fp / s_out).astype(np.float32)
+    y, _ = oracle.conv_fwd_int8(x, w, scale, bias, imap)
+    real = oracle.conv_fwd(x.astype(np.float64) * float(s_in),
+                           w.astype(np.float64) * s_w.astype(np.float64)[None, None, :],
+                           bias_fp, imap) / float(s_out)
+    q = np.clip(np.where(real >= 0, np.floor(real + 0.5), np.ceil(real - 0.5)), -128, 127)
+    diff = np.abs(y.astype(np.int64) - q.astype(np.int64))
+    assert diff.max() <= 1
+    near_tie = np.abs(np.abs(real - np.trunc(real)) - 0.5) < 1e-3
+    assert np.all(near_tie[diff > 0])
+    assert (diff == 0).mean() > 0.99
+    assert np.unique(y).size > 50  # the case spans the code range
+
+
+def test_int8_residual_relu_translation():
+    """ReLU output is nonnegative, saturated codes sit at the ends, and a
+    translated scene gives the same codes."""
+    coords, imap, x, w, g = _int8_case(14, cin=8, cout=8)
+    add = g.integers(-128, 128, size=(coords.shape[0], 8)).astype(np.int8)
+    sc = np.full(8, 0.003, np.float32)
+    y, acc = oracle.conv_fwd_int8(x, w, sc, None, imap, add=add, add_scale=0.5, relu=True)
+    assert y.min() >= 0
+    shifted = coords.copy()
+    shifted[:, 1:] += 1
+    imap2, _ = oracle.subm_map(shifted, 2, (8, 9, 10))
+    y2, acc2 = oracle.conv_fwd_int8(x, w, sc, None, imap2, add=add, add_scale=0.5, relu=True)
+    assert np.array_equal(y, y2) and np.array_equal(acc, acc2)
