@@ -71,8 +71,10 @@ DESCRIPTIONS = {
                              "(maps built once), 256^3 shell, bf16 128 channels",
     "shell256_inverse_bf16": "SparseInverseConv3d of a k3 s2 p1 conv (maps and row order "
                              "built once), 256^3 shell, bf16 128->128",
+    "shell256_int8": "quantized SubMConv3d k3 indice build + int8 forward (per-channel scale and "
+                     "bias, ReLU, int8 out), 256^3 shell, int8 128->128",
 }
-ELEM = {"f32": 4, "f16": 2, "bf16": 2}
+ELEM = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
 
 
 def peaks():
@@ -281,6 +283,26 @@ class Case:
                     kernels="k_build_init, k_hash_insert, k_map_probe<imap_t>", launches=3))
         n_out, P = self.n_out, self.pairs
         self.imap, self.mask = imap, mask
+        if w.get("int8"):
+            # quantized layer: int8 codes in and out, exact integer sums on the
+            # fp16 tensor cores (weights split into 4-bit halves per call)
+            self.inverse = self.maxpool = self.train = False
+            self.int8 = True
+            self.scale, self.qbias = w["scale"].to(dev), w["bias"].to(dev)
+            self.bias = None
+            self.y = torch.empty((n_out, cout), dtype=torch.int8, device=dev)
+            nbw = int(B.lib().spc_conv_int8_workspace_size(K, cin, cout))
+            self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
+            self.phases.append(Phase(
+                "fwd", lambda: spc.spc_conv_fwd_int8(self.x, self.wt, self.scale, self.qbias,
+                                                     self.imap, self.mask, act=B.SPC_ACT_RELU,
+                                                     out=self.y, status=self.status,
+                                                     ws=self.conv_ws),
+                "conv", n * cin + n_out * cout + K * cin * cout + 4 * P + 8 * cout,
+                2.0 * P * cin * cout, kernels="k_i8_split_w + k_conv_i8 (tcgen05, fp16 halves)",
+                launches=2))
+            return
+        self.int8 = False
         if w.get("maxpool"):
             # pooling on the strided map of its window: forward with argmax, then
             # the input gradient through the transposed map
@@ -414,6 +436,10 @@ class Case:
         elif self.inverse:
             # the maps are saved from the strided conv: a step moves features and weights
             ins = [("yin", self.yin.cpu()), ("wt", self.w["w"])]
+            outs = ["y"]
+        elif self.int8:
+            ins = [("coords", self.coords_h), ("x", self.w["x"]), ("wt", self.w["w"]),
+                   ("scale", self.w["scale"]), ("qbias", self.w["bias"])]
             outs = ["y"]
         else:
             ins = [("coords", self.coords_h), ("x", self.w["x"]), ("wt", self.w["w"])]
@@ -576,7 +602,7 @@ def record_traffic(csv_path: str, workload: str, phases):
         got["build"] = per_call(k(r"k_(build_init|hash_insert|map_probe)"), r"k_map_probe")
     conv = k(r"k_(conv_|gather_gemm)")
     fwd, dgr = (conv[0::2], conv[1::2]) if "dgrad" in phases else (conv, [])
-    tr = k(r"k_transpose_w")
+    tr = k(r"k_(transpose_w|i8_split_w)")
     if fwd:
         got["inverse" if "inverse" in phases else "fwd"] = sum(d["bytes"] for d in fwd) / len(fwd) + (
             sum(d["bytes"] for d in tr) / len(tr) if tr else 0.0)
@@ -612,6 +638,10 @@ def roofline(p: Phase, ms: float, hbm: float, tc_peak: float, alu_peak: float, d
     else:
         if dtype == "f32" and not prec_tf32:
             cpeak, cbound = alu_peak, "alu"
+        elif dtype == "i8":
+            # no integer MMA on sm_103a: each int8 multiply-add is two fp16 ones
+            # (the weight's two 4-bit halves), so half the 16-bit tensor peak
+            cpeak, cbound = tc_peak / 2.0, "tensor"
         else:
             cpeak, cbound = (tc_peak * (1.1 / 2.25) if dtype == "f32" else tc_peak), "tensor"
         t_c = p.flops / (cpeak * 1e12)
@@ -711,7 +741,7 @@ def run_ours(args, rank, world, local, dist):
         "roofline": {"kernel": f"{dom.name}: {dom.kernels}", "bound": dom_r["bound"],
                      "achieved": dom_r["achieved"], "peak": dom_r["peak"], "unit": dom_r["unit"],
                      "frac": dom_r["frac"], "traffic": measured_traffic(args.workload, dom.name),
-                     "peak_source": f"{peak_src} ({'hbm_gbs burst copy' if dom_r['unit'] == 'GB/s' else 'bf16_tflops burst' if dom_r['bound'] == 'tensor' else 'FP32 lanes x clock'})",
+                     "peak_source": f"{peak_src} ({'hbm_gbs burst copy' if dom_r['unit'] == 'GB/s' else ('bf16_tflops burst / 2: int8 runs as two fp16 products' if case.dtype == 'i8' else 'bf16_tflops burst') if dom_r['bound'] == 'tensor' else 'FP32 lanes x clock'})",
                      "alg_bytes_per_launch": dom.bytes_alg, "alg_flops_per_launch": dom.flops},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(case.h2d),
@@ -724,6 +754,18 @@ def run_ours(args, rank, world, local, dist):
     return line
 
 
+_THREADS = [1]  # oracle threads of the current sample (for its description)
+
+
+def oracle_threads(n: int) -> int:
+    """Sets the oracle's row-loop threads; returns the count in effect."""
+    import oracle
+
+    oracle.build()
+    _THREADS[0] = oracle.set_threads(n)
+    return _THREADS[0]
+
+
 def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, pad=0):
     """Times the oracle on a bounded sample; returns (TFLOP/s, description)."""
     import oracle
@@ -731,8 +773,9 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
     oracle.build()
     c = case_w["coords"]
     n = c.shape[0]
-    x64, w64 = oracle.f64(case_w["x"]), oracle.f64(case_w["w"])
-    b64 = oracle.f64(case_w["bias"]) if case_w["bias"] is not None else None
+    if not case_w.get("int8"):
+        x64, w64 = oracle.f64(case_w["x"]), oracle.f64(case_w["w"])
+        b64 = oracle.f64(case_w["bias"]) if case_w["bias"] is not None else None
     cin, cout = case_w["cin"], case_w["cout"]
     t0 = time.perf_counter()
     if subm:
@@ -748,7 +791,19 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
         t = time.perf_counter() - t1
         return float(cnt.sum()) * cin / t / 1e12, (f"fp64 max pool of all {imap.shape[1]} output "
                                                    f"rows (map built once, not charged), {t:.1f} s, "
-                                                   f"single thread")
+                                                   f"{_THREADS[0]} thread(s)")
+    if case_w.get("int8"):
+        # the oracle's int8 rule on a sample of output rows (the map charged pro rata)
+        per_row = 2.0 * float(cnt.sum()) / max(n, 1) * cin * cout
+        rows = int(min(n, max(64, budget_s * 0.5e9 / max(per_row, 1.0))))
+        sel = np.linspace(0, n - 1, rows).astype(np.int64)
+        t1 = time.perf_counter()
+        oracle.conv_fwd_int8(case_w["x"], case_w["w"], case_w["scale"], case_w["bias"],
+                             imap[:, sel], relu=True)
+        t = time.perf_counter() - t1 + t_map * rows / max(n, 1)
+        flops = 2.0 * float((imap[:, sel] >= 0).sum()) * cin * cout
+        return flops / t / 1e12, (f"map over all {n} voxels ({t_map:.2f} s, charged pro rata) + "
+                                  f"int8 forward of {rows} of {n} rows, {t:.1f} s, {_THREADS[0]} thread(s)")
     if case_w.get("inverse"):
         # the inverse conv on the saved maps (not charged): the oracle's forward
         # gathered through the transposed map (the same sums; the oracle pins
@@ -765,7 +820,7 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
         flops = 2.0 * float((imap_t[:, sel] >= 0).sum()) * cin * cout
         return flops / t / 1e12, (f"fp64 inverse conv (gather through the transposed map) of {rows} "
                                   f"of {n} output rows (maps built once, not charged), {t:.1f} s, "
-                                  f"single thread")
+                                  f"{_THREADS[0]} thread(s)")
     n_out = imap.shape[1]
     per_row = 2.0 * float(cnt.sum()) / max(n_out, 1) * cin * cout  # flops per output row
     # rows so that the forward sample takes about the budget at ~1 GFLOP/s
@@ -789,15 +844,23 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
     what = (f"{reps} whole steps (map + fp64 forward of all {n_out} rows)" if sel is None else
             f"map over all {n} voxels ({t_map:.2f} s, charged pro rata) + fp64 forward of "
             f"{len(sel)} of {n_out} rows")
-    return flops / t / 1e12, f"{what}, {t:.1f} s, single thread"
+    return flops / t / 1e12, f"{what}, {t:.1f} s, {_THREADS[0]} thread(s)"
 
 
 def cpu_baseline(case, budget_s=10.0):
+    """The oracle on the host cores: one thread, then one thread per core (its
+    row loops run in parallel; the results do not depend on the count)."""
     w = case.w
-    val, what = cpu_sample(w, case.batch, case.shape, case.ks, w["subm"], case.pairs, budget_s,
-                           w.get("stride", 1), w.get("pad", 0))
-    return {"value": round(val, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": what}
+    args = (w, case.batch, case.shape, case.ks, w["subm"], case.pairs, budget_s / 2,
+            w.get("stride", 1), w.get("pad", 0))
+    oracle_threads(1)
+    v1, what1 = cpu_sample(*args)
+    cores = oracle_threads(os.cpu_count() or 1)
+    vn, whatn = cpu_sample(*args)
+    oracle_threads(1)
+    return {"value": round(vn, 8), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": whatn,
+            "single_thread": {"value": round(v1, 8), "cores": 1, "sample": what1}}
 
 
 def run_reference(args, rank, world):
@@ -809,6 +872,7 @@ def run_reference(args, rank, world):
     c = w["coords"]
     batch = int(c[:, 0].max()) + 1
     vals = []
+    cores = oracle_threads(os.cpu_count() or 1)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         v, what = cpu_sample(w, batch, shape, w["k"], w["subm"], None,
@@ -821,11 +885,12 @@ def run_reference(args, rank, world):
         "impl": "reference",
         "metric": METRIC, "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8" if w.get("int8") else "f64",
         "data": "synthetic (seeded scene, random-init weights)",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
                    "n_voxels": int(c.shape[0])},
-        "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: {what}"},
         "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -67,7 +67,7 @@ typedef enum {
     SPC_ERR_UNSUPPORTED = 6,   /* a valid request this build does not implement */
     SPC_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch, copy) */
     SPC_ERR_WORKSPACE = 8,     /* workspace missing or smaller than required */
-    SPC_ERR_TIMEOUT = 9        /* an internal GPU wait exceeded its bound (2 s); results invalid */
+    SPC_ERR_TIMEOUT = 9        /* an internal GPU wait exceeded its bound (spc_set_wait_limit_ns); results invalid */
 } spc_status;
 
 typedef enum { SPC_F32 = 0, SPC_F16 = 1, SPC_BF16 = 2 } spc_dtype;
@@ -104,6 +104,21 @@ SPC_API const char* spc_status_string(spc_status s);
 
 /* Library version as major*10000 + minor*100 + patch. */
 SPC_API int32_t spc_version(void);
+
+/* Bound on the waits inside the pipelined tensor-core kernels (conv forward,
+ * dinput, inverse, dfilter) of one warp role on another: a gather warp waiting
+ * for a free stage, the MMA thread waiting for a full one.  Such a wait never
+ * lasts long in a healthy run; one that runs out makes the kernel set
+ * SPC_ERR_TIMEOUT in the call's status word, wait for the copies and MMAs it
+ * issued itself (those always finish; bounded by 2 s), free its tensor memory
+ * and return, so the context stays usable.  The limit applies to kernels
+ * launched (or captured into a graph) after the call; process-wide; default
+ * 2,000,000,000 ns, at most 60 s (SPC_ERR_INVALID_ARG above).  A limit of 0
+ * gives up at the first such wait whose phase is not already complete.  The
+ * limit is checked between suspended polls of up to 100 us, so a wait may run
+ * past it by that much. */
+SPC_API spc_status spc_set_wait_limit_ns(uint64_t ns);
+SPC_API uint64_t spc_get_wait_limit_ns(void);
 
 /* Output grid of a strided (regular) sparse conv, per axis
  * floor((in + 2 pad - dil (k - 1) - 1) / stride) + 1, or 0 when the window never
@@ -225,8 +240,10 @@ SPC_API spc_status spc_strided_out_coords(const int32_t* coords, int64_t n_in, i
  *        one burst and skips the offsets no row of its tile uses).
  *  y     [n_out, cout] of dtype dt out (fp32 accumulate, one rounding).
  *  status  device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
- *  ws    spc_conv_workspace_size(...) bytes (the tensor-core path keeps the
- *        weights transposed to [K, Cout, Cin] there).
+ *  ws    spc_conv_workspace_size(...) bytes: 0 when the tensor-core path reads
+ *        W as stored (fp16 / bf16 with Cin and Cout multiples of 64); the
+ *        other tensor-core shapes keep the weights transposed to [K, Cout, Cin]
+ *        there.
  *  x, w, y must be 16-byte aligned.
  *  Kernels: a one-row-per-thread kernel when Cin and Cout are both in
  *  {8, 16, 32} (narrow layers on sparse scenes are latency-bound); else
@@ -296,6 +313,50 @@ SPC_API spc_status spc_conv_inverse(const void* y, const void* w, const void* bi
                                     int32_t cy, int32_t cout, spc_dtype dt, spc_precision prec,
                                     void* out, int32_t* status, void* ws, size_t ws_bytes,
                                     void* stream);
+
+/* spc_conv_fwd_int8 -- quantized forward, spconv's int8 implicit GEMM (spconv
+ * docs, TENSORRT_INT8_GUIDE.md: "Spconv Int8 Scale/Bias Conversion Basic Rule",
+ * fp32 = int8 * scale and int8 = saturate(round(fp32 / scale)); "Call Spconv
+ * Implicit GEMM with Calculated Scales and Bias"; "Calculate Spconv Int8 Scale
+ * and Bias from PyTorch Quantized Layer", scale = input_scale *
+ * weight_scale[j] / output_scale and bias = bias_fp / output_scale):
+ *   acc[o, j] = sum over pairs (k, i = imap[k, o] != -1) of sum_c x[i, c] w[k, c, j]
+ *               (exact integer sum),
+ *   f = float(acc) * scale[j] + bias[j] + add_scale * float(add[o, j]),
+ *   f = max(f, 0) with SPC_ACT_RELU,
+ *   y[o, j] = saturate(round(f)) to [-128, 127], round half away from zero;
+ * each fp32 operation rounded once in that order (nothing fused), so the codes
+ * are bit-exact against a CPU evaluation of the same expression.
+ * sm_103a has no integer tensor-core MMA; the sums are formed exactly on the
+ * fp16 tensor cores (int8 values are exact in fp16; each weight is split into
+ * two 4-bit halves so every fp32 partial sum is an exact integer), which needs
+ * K * cin <= 8192.
+ *
+ *  x      [n_in, cin] int8.   w [K, cin, cout] int8.
+ *  scale  [cout] fp32 (device).   bias [cout] fp32 (device) or NULL.
+ *  imap   [K, n_out] int32, or NULL when K == 1 and n_in == n_out.
+ *  mask, perm  [n_out] uint32 / int32 from spc_map_row_order(imap), or NULL:
+ *         with them tiles of rows grouped by offset mask run only their
+ *         offsets (spconv's do_sort); NULL keeps rows in map order (do_sort =
+ *         false, "Optimize Int8 Kernels by Disabling Sort in Implicit Gemm").
+ *         The result is the same either way.
+ *  add    [n_out, cout] int8 residual (16-byte aligned, not y) or NULL;
+ *         add_scale its fp32 scale relative to the output.
+ *  act    SPC_ACT_NONE or SPC_ACT_RELU.
+ *  y      [n_out, cout] int8 out.
+ *  status device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
+ *  ws     spc_conv_int8_workspace_size(K, cin, cout) bytes, 256-byte aligned
+ *         (the split weights, fp16 [K, 2 cout, cin]).
+ *  x, w, y must be 16-byte aligned.  cin and cout multiples of 64, K <= 32 and
+ *  K * cin <= 8192, else SPC_ERR_UNSUPPORTED (the workspace size is then 0).
+ */
+SPC_API size_t spc_conv_int8_workspace_size(int32_t K, int32_t cin, int32_t cout);
+SPC_API spc_status spc_conv_fwd_int8(const int8_t* x, const int8_t* w, const float* scale,
+                                     const float* bias, const int32_t* imap, const uint32_t* mask,
+                                     const int32_t* perm, int32_t K, int64_t n_in, int64_t n_out,
+                                     int32_t cin, int32_t cout, const int8_t* add, float add_scale,
+                                     spc_activation act, int8_t* y, int32_t* status, void* ws,
+                                     size_t ws_bytes, void* stream);
 
 /* spc_map_row_order -- the rows of a map [K, n] grouped by offset mask.
  * mask[i] gets bit k when map[k, i] != -1, and perm lists the rows sorted by

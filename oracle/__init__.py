@@ -42,8 +42,11 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
+        cmd = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC,
+               "-lm"]
+        # row loops in parallel where the compiler has OpenMP; plain C otherwise
+        if subprocess.run(cmd[:1] + ["-fopenmp"] + cmd[1:], capture_output=True).returncode != 0:
+            subprocess.check_call(cmd)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -95,11 +98,19 @@ def _load():
             lib.orc_conv_wgrad_entries.restype = None
             _I8P = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
             _F32P = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+            lib.orc_set_threads.argtypes = [_i32]
+            lib.orc_set_threads.restype = _i32
             lib.orc_conv_fwd_int8.argtypes = [_I8P, _I8P, _F32P, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_float, _i32, ctypes.c_void_p, _i64, _i64,
                                               _i64, _i32, _i32, _I8P, _I32P]
             _lib = lib
     return _lib
+
+
+def set_threads(n: int = 0) -> int:
+    """Threads of the oracle's parallel row loops (n > 0 sets them); returns the
+    count in effect (1 when it was compiled without OpenMP)."""
+    return int(_load().orc_set_threads(int(n)))
 
 
 def _triple(v) -> np.ndarray:

@@ -36,11 +36,19 @@
  *    the HYGON-AI spconv-das README, Testing and Accuracy.)
  *
  * All floating point is double precision on the exact input values.
+ *
+ * Output rows are independent sums, so the row loops of the map probe and of
+ * the forward run as OpenMP parallel loops when the file is compiled with
+ * OpenMP (each row is still computed by one thread in the order written, so the
+ * results do not depend on the thread count); orc_set_threads picks the count.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_OK 0
 #define ORC_ERR_RANGE 1
@@ -53,6 +61,19 @@ typedef struct {
     int64_t key;
     int64_t row;
 } orc_entry;
+
+/* Threads of the parallel row loops (n > 0 sets them); returns the count in
+ * effect, 1 without OpenMP. */
+int orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
 
 static int cmp_entry(const void* a, const void* b)
 {
@@ -146,6 +167,7 @@ int orc_subm_map(const int32_t* coords, int64_t n, int32_t batch, const int32_t 
         int64_t d[3];
         for (int a = 0; a < 3; ++a) d[a] = (abc[a] - ksize[a] / 2) * dil[a];
         int64_t hits = 0;
+#pragma omp parallel for schedule(static) reduction(+ : hits)
         for (int64_t o = 0; o < n; ++o) {
             const int32_t* c = coords + 4 * o;
             int64_t z = c[1] + d[0], y = c[2] + d[1], x = c[3] + d[2];
@@ -310,6 +332,7 @@ void orc_conv_fwd(const double* x, const double* w, const double* bias, const in
                   int64_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout, double* y)
 {
     (void)n_in;
+#pragma omp parallel for schedule(dynamic, 64)
     for (int64_t o = 0; o < n_out; ++o) fwd_row(x, w, bias, imap, K, n_out, cin, cout, o, y + o * cout);
 }
 
@@ -319,6 +342,7 @@ void orc_conv_fwd_rows(const double* x, const double* w, const double* bias, con
                        const int64_t* rows, int64_t n_rows, double* y_rows)
 {
     (void)n_in;
+#pragma omp parallel for schedule(dynamic, 64)
     for (int64_t r = 0; r < n_rows; ++r)
         fwd_row(x, w, bias, imap, K, n_out, cin, cout, rows[r], y_rows + r * cout);
 }
@@ -503,45 +527,60 @@ void orc_conv_wgrad_entries(const double* x, const double* dy, const int32_t* im
  * (nullable) receives the integer sums.  Returns ORC_ERR_ARG if a sum leaves
  * the 32-bit range.
  */
+/* One output row of the int8 rule; returns 1 if a sum leaves the 32-bit range. */
+static int fwd_int8_row(const int8_t* x, const int8_t* w, const float* scale, const float* bias,
+                        const int8_t* add, float add_scale, int32_t relu, const int32_t* imap,
+                        int64_t K, int64_t n_out, int32_t cin, int32_t cout, int64_t o, int64_t* acc,
+                        int8_t* yo, int32_t* acc_o)
+{
+    for (int32_t j = 0; j < cout; ++j) acc[j] = 0;
+    for (int64_t k = 0; k < K; ++k) {
+        int32_t i = imap ? imap[k * n_out + o] : (int32_t)o;
+        if (i < 0) continue;
+        const int8_t* xi = x + (int64_t)i * cin;
+        const int8_t* wk = w + k * cin * cout;
+        for (int32_t c = 0; c < cin; ++c)
+            for (int32_t j = 0; j < cout; ++j) acc[j] += (int64_t)xi[c] * (int64_t)wk[(int64_t)c * cout + j];
+    }
+    for (int32_t j = 0; j < cout; ++j) {
+        if (acc[j] > INT32_MAX || acc[j] < INT32_MIN) return 1;
+        if (acc_o) acc_o[j] = (int32_t)acc[j];
+        float f = (float)(int32_t)acc[j];
+        f = f * scale[j];
+        if (bias) f = f + bias[j];
+        if (add) {
+            float t = add_scale * (float)add[o * cout + j];
+            f = f + t;
+        }
+        if (relu && f < 0.0f) f = 0.0f;
+        float r = roundf(f);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -128.0f) r = -128.0f;
+        yo[j] = (int8_t)r;
+    }
+    return 0;
+}
+
 int orc_conv_fwd_int8(const int8_t* x, const int8_t* w, const float* scale, const float* bias,
                       const int8_t* add, float add_scale, int32_t relu, const int32_t* imap,
                       int64_t K, int64_t n_in, int64_t n_out, int32_t cin, int32_t cout, int8_t* y,
                       int32_t* acc_out)
 {
     (void)n_in;
-    int64_t* acc = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cout > 0 ? cout : 1));
-    if (!acc) return ORC_ERR_NOMEM;
-    for (int64_t o = 0; o < n_out; ++o) {
-        for (int32_t j = 0; j < cout; ++j) acc[j] = 0;
-        for (int64_t k = 0; k < K; ++k) {
-            int32_t i = imap ? imap[k * n_out + o] : (int32_t)o;
-            if (i < 0) continue;
-            const int8_t* xi = x + (int64_t)i * cin;
-            const int8_t* wk = w + k * cin * cout;
-            for (int32_t c = 0; c < cin; ++c)
-                for (int32_t j = 0; j < cout; ++j)
-                    acc[j] += (int64_t)xi[c] * (int64_t)wk[(int64_t)c * cout + j];
-        }
-        for (int32_t j = 0; j < cout; ++j) {
-            if (acc[j] > INT32_MAX || acc[j] < INT32_MIN) {
-                free(acc);
-                return ORC_ERR_ARG;
-            }
-            if (acc_out) acc_out[o * cout + j] = (int32_t)acc[j];
-            float f = (float)(int32_t)acc[j];
-            f = f * scale[j];
-            if (bias) f = f + bias[j];
-            if (add) {
-                float t = add_scale * (float)add[o * cout + j];
-                f = f + t;
-            }
-            if (relu && f < 0.0f) f = 0.0f;
-            float r = roundf(f);
-            if (r > 127.0f) r = 127.0f;
-            if (r < -128.0f) r = -128.0f;
-            y[o * cout + j] = (int8_t)r;
+    int bad = 0;
+#pragma omp parallel reduction(| : bad)
+    {
+        int64_t* acc = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cout > 0 ? cout : 1));
+        if (!acc) {
+            bad |= 2;
+        } else {
+#pragma omp for schedule(dynamic, 64)
+            for (int64_t o = 0; o < n_out; ++o)
+                bad |= fwd_int8_row(x, w, scale, bias, add, add_scale, relu, imap, K, n_out, cin,
+                                    cout, o, acc, y + o * cout, acc_out ? acc_out + o * cout : NULL);
+            free(acc);
         }
     }
-    free(acc);
-    return ORC_OK;
+    if (bad & 2) return ORC_ERR_NOMEM;
+    return bad ? ORC_ERR_ARG : ORC_OK;
 }

@@ -219,7 +219,18 @@ WORKLOADS = {
     "shell256_inverse_bf16": dict(coords=("shell256",), batch=1, shape=(256, 256, 256), k=3,
                                   stride=2, pad=1, subm=False, dtype="bf16", cin=128, cout=128,
                                   bias_var=None, seed=9, inverse=True),
+    # quantized inference layer on the 256^3 shell: int8 codes in and out, fp32
+    # per-channel scale and bias, ReLU
+    "shell256_int8": dict(coords=("shell256",), batch=1, shape=(256, 256, 256), k=3, stride=1,
+                          pad=1, subm=True, dtype="i8", cin=128, cout=128, bias_var=None, seed=12,
+                          int8=True),
 }
+
+
+def int8_codes(shape, std: float, seed: int, tag: int) -> torch.Tensor:
+    """Integer codes rint(N(0, std^2)) clipped to [-128, 127], as int8 (CPU)."""
+    a = np.clip(np.rint(rng(seed, tag).standard_normal(shape) * std), -128, 127)
+    return torch.from_numpy(a.astype(np.int8))
 
 _COORD_CACHE: dict = {}
 
@@ -257,6 +268,18 @@ def workload(name: str) -> dict:
     out = dict(spec)
     out["name"] = name
     out["coords"] = coords
+    if spec.get("int8"):
+        # codes of std 32 (features) and 24 (weights); per-channel output scales
+        # put the integer sums' typical size (about 32 * 24 * sqrt(20 Cin) on the
+        # shells' ~20 pairs per voxel) at about 40 codes; bias of a few codes
+        out["x"] = int8_codes((n, cin), 32.0, seed, 1)
+        out["w"] = int8_codes((K, cin, cout), 24.0, seed, 2)
+        g = rng(seed, 3)
+        typical = 32.0 * 24.0 * np.sqrt(20.0 * cin)
+        out["scale"] = torch.from_numpy((g.uniform(0.5, 1.5, size=cout) * 40.0 / typical)
+                                        .astype(np.float32))
+        out["bias"] = torch.from_numpy(g.normal(0.0, 4.0, size=cout).astype(np.float32))
+        return out
     out["x"] = normal((n, cin), 1.0, dt, seed, 1)
     out["w"] = normal((K, cin, cout), float(np.sqrt(1.0 / (27 * cin))), dt, seed, 2)
     out["bias"] = (normal((cout,), float(np.sqrt(spec["bias_var"])), dt, seed, 3)

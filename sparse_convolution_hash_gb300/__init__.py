@@ -19,6 +19,9 @@ from .binding import (  # noqa: F401
     spc_conv_dgrad,
     spc_conv_fwd,
     spc_conv_fwd_fused,
+    spc_conv_fwd_int8,
+    spc_get_wait_limit_ns,
+    spc_set_wait_limit_ns,
     SPC_ACT_NONE,
     SPC_ACT_RELU,
     spc_conv_inverse,

@@ -90,6 +90,10 @@ def lib():
             L.spc_status_string.restype = ctypes.c_char_p
             L.spc_version.argtypes = []
             L.spc_version.restype = _i32
+            L.spc_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.spc_set_wait_limit_ns.restype = _i32
+            L.spc_get_wait_limit_ns.argtypes = []
+            L.spc_get_wait_limit_ns.restype = ctypes.c_uint64
             L.spc_out_shape.argtypes = [_I3, _GP, _I3]
             L.spc_out_shape.restype = _i32
             L.spc_indice_map_workspace_size.argtypes = [_i64]
@@ -121,6 +125,11 @@ def lib():
             L.spc_map_row_order.argtypes = [_p, _i32, _i64, _p, _p, _p, _sz, _p]
             L.spc_map_row_order.restype = _i32
             L.spc_conv_inverse.restype = _i32
+            L.spc_conv_int8_workspace_size.argtypes = [_i32, _i32, _i32]
+            L.spc_conv_int8_workspace_size.restype = _sz
+            L.spc_conv_fwd_int8.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32,
+                                            _p, ctypes.c_float, _i32, _p, _p, _p, _sz, _p]
+            L.spc_conv_fwd_int8.restype = _i32
             L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _i32, _i64, _i64, _i32, _i32,
                                          _i32, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_dgrad.restype = _i32
@@ -174,6 +183,17 @@ def spc_status_string(code: int) -> str:
 
 def spc_version() -> int:
     return int(lib().spc_version())
+
+
+def spc_set_wait_limit_ns(ns: int) -> None:
+    """Bound (ns) of the waits of one warp role on another in the pipelined
+    tensor-core kernels launched afterwards (a wait that runs out sets
+    SPC_ERR_TIMEOUT in the call's status word)."""
+    _check(lib().spc_set_wait_limit_ns(int(ns)), "spc_set_wait_limit_ns")
+
+
+def spc_get_wait_limit_ns() -> int:
+    return int(lib().spc_get_wait_limit_ns())
 
 
 def spc_out_shape(in_shape, ksize=3, stride=2, pad=1, dil=1) -> tuple:
@@ -396,6 +416,40 @@ def spc_conv_inverse(y: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tens
                                   _stream(y.device))
     _check(code, "spc_conv_inverse")
     return o
+
+
+def spc_conv_fwd_int8(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor,
+                      bias: Optional[torch.Tensor], imap: Optional[torch.Tensor],
+                      mask: Optional[torch.Tensor] = None, perm: Optional[torch.Tensor] = None,
+                      add: Optional[torch.Tensor] = None, add_scale: float = 0.0,
+                      act: int = SPC_ACT_NONE, n_out: Optional[int] = None,
+                      out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                      ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quantized forward: int8 x [n_in, cin], int8 w [K, cin, cout], fp32 per-channel
+    scale and bias, optional int8 residual `add` with `add_scale`, optional ReLU;
+    returns int8 [n_out, cout].  `perm` / `mask` from spc_map_row_order(imap)
+    group rows by offset mask (spconv's do_sort); None keeps map order."""
+    x = _cuda(x, "x")
+    w = _cuda(w, "w")
+    assert x.dtype == torch.int8 and w.dtype == torch.int8
+    sc = _cuda(scale, "scale").to(torch.float32).contiguous()
+    b = _cuda(bias, "bias").to(torch.float32).contiguous() if bias is not None else None
+    K, cin, cout = w.shape
+    if imap is not None:
+        imap = _cuda(imap, "imap")
+        n_out = imap.shape[1]
+    elif n_out is None:
+        n_out = x.shape[0]
+    y = torch.empty((n_out, cout), dtype=torch.int8, device=x.device) if out is None else out
+    nbytes = int(lib().spc_conv_int8_workspace_size(K, cin, cout))
+    if ws is None or ws.numel() < nbytes:
+        ws = _workspace(max(nbytes, 256), x.device)
+    code = lib().spc_conv_fwd_int8(_ptr(x), _ptr(w), _ptr(sc), _ptr(b), _ptr(imap), _ptr(mask),
+                                   _ptr(perm), K, x.shape[0], n_out, cin, cout, _ptr(add),
+                                   float(add_scale), act, _ptr(y), _ptr(status), _ptr(ws),
+                                   ws.numel(), _stream(x.device))
+    _check(code, "spc_conv_fwd_int8")
+    return y
 
 
 def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tensor], kind: int,

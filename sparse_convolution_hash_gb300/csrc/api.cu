@@ -4,9 +4,17 @@
 // anything is enqueued), carves the caller's workspace, and enqueues its
 // kernels on the caller's stream.  Nothing here allocates device memory or
 // synchronises.
+#include <atomic>
+
 #include "kernels.cuh"
 
 using namespace spc;
+
+namespace {
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+}  // namespace
+
+uint64_t spc::wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -61,6 +69,15 @@ const char* spc_status_string(spc_status s)
 }
 
 int32_t spc_version(void) { return kVersion; }
+
+spc_status spc_set_wait_limit_ns(uint64_t ns)
+{
+    if (ns > 60000000000ull) return SPC_ERR_INVALID_ARG;
+    g_wait_ns.store(ns, std::memory_order_relaxed);
+    return SPC_OK;
+}
+
+uint64_t spc_get_wait_limit_ns(void) { return wait_limit_ns(); }
 
 spc_status spc_out_shape(const int32_t in_shape[3], const spc_geom* g, int32_t out_shape[3])
 {
@@ -201,8 +218,11 @@ size_t spc_conv_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t c
     (void)n_in;
     (void)n_out;
     if (K < 1 || cin < 1 || cout < 1 || !dtype_ok(dt)) return 0;
-    if (conv_tc_supported(cin, cout, K, dt, SPC_PREC_EXACT) ||
-        conv_tc_supported(cin, cout, K, dt, SPC_PREC_TF32))
+    // the tensor-core forward needs a transposed copy of the weights unless it
+    // reads them as stored
+    if ((conv_tc_supported(cin, cout, K, dt, SPC_PREC_EXACT) ||
+         conv_tc_supported(cin, cout, K, dt, SPC_PREC_TF32)) &&
+        !conv_tc_reads_w_as_stored(cin, cout, dt))
         return conv_tc_weight_bytes(K, cin, cout, dt);
     return 0;
 }
@@ -274,14 +294,19 @@ spc_status conv_fwd_impl(const void* x, const void* w, const void* bias, const i
     // would mostly multiply zero-filled rows)
     const bool narrow = conv_narrow_supported(cin, cout, K, dt);
     if (n_out > 0 && !narrow && conv_tc_supported(cin, cout, K, dt, prec) && aligned16(x) && aligned16(y)) {
-        const size_t wbytes = conv_tc_weight_bytes(K, cin, cout, dt);
-        if (!ws || ws_bytes < wbytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
-            return SPC_ERR_WORKSPACE;
-        s = transpose_weights(w, ws, K, cin, cout, dt, st);
-        if (s != SPC_OK) return s;
+        // 16-bit rows of multiples of 64 channels read W[k] as stored (an
+        // MN-major operand); the other shapes take it transposed in the workspace
+        const bool b_mn = conv_tc_reads_w_as_stored(cin, cout, dt);
+        if (!b_mn) {
+            const size_t wbytes = conv_tc_weight_bytes(K, cin, cout, dt);
+            if (!ws || ws_bytes < wbytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+                return SPC_ERR_WORKSPACE;
+            s = transpose_weights(w, ws, K, cin, cout, dt, st);
+            if (s != SPC_OK) return s;
+        }
         TcArgs a;
         a.in = x;
-        a.b = ws;
+        a.b = b_mn ? w : ws;
         a.bias = bias;
         a.map = imap;
         a.mask = mask;
@@ -297,6 +322,8 @@ spc_status conv_fwd_impl(const void* x, const void* w, const void* bias, const i
         a.residual = residual;
         a.add_scale = add_scale;
         a.act = (int32_t)act;
+        a.b_mn = b_mn ? 1 : 0;
+        a.wait_ns = wait_limit_ns();
         s = conv_gather_tc(a, dt, st);
         if (s != SPC_ERR_UNSUPPORTED) return s;
     }
@@ -322,6 +349,53 @@ spc_status spc_conv_fwd(const void* x, const void* w, const void* bias, const in
 {
     return conv_fwd_impl(x, w, bias, imap, mask, nullptr, K, n_in, n_out, cin, cout, dt, prec,
                          nullptr, 0.f, SPC_ACT_NONE, y, status, ws, ws_bytes, stream);
+}
+
+size_t spc_conv_int8_workspace_size(int32_t K, int32_t cin, int32_t cout)
+{
+    if (!conv_i8_supported(K, cin, cout)) return 0;
+    return conv_i8_ws_bytes(K, cin, cout);
+}
+
+spc_status spc_conv_fwd_int8(const int8_t* x, const int8_t* w, const float* scale,
+                             const float* bias, const int32_t* imap, const uint32_t* mask,
+                             const int32_t* perm, int32_t K, int64_t n_in, int64_t n_out,
+                             int32_t cin, int32_t cout, const int8_t* add, float add_scale,
+                             spc_activation act, int8_t* y, int32_t* status, void* ws,
+                             size_t ws_bytes, void* stream)
+{
+    if (K < 1 || n_in < 0 || n_out < 0 || cin < 1 || cout < 1) return SPC_ERR_INVALID_ARG;
+    if (act != SPC_ACT_NONE && act != SPC_ACT_RELU) return SPC_ERR_INVALID_ARG;
+    if (!w || !aligned16(w) || !scale) return SPC_ERR_INVALID_ARG;
+    if (n_in > 0 && (!x || !aligned16(x))) return SPC_ERR_INVALID_ARG;
+    if (n_out > 0 && (!y || !aligned16(y))) return SPC_ERR_INVALID_ARG;
+    if (add && (!aligned16(add) || add == y)) return SPC_ERR_INVALID_ARG;
+    if (!imap && n_out > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
+    if ((mask || perm) && K > 32) return SPC_ERR_INVALID_ARG;
+    if (n_in > INT32_MAX - 1 || n_out > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
+    if (!conv_i8_supported(K, cin, cout)) return SPC_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < conv_i8_ws_bytes(K, cin, cout) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return SPC_ERR_WORKSPACE;
+    I8Args a;
+    a.in = x;
+    a.wq = static_cast<__half*>(ws);
+    a.scale = scale;
+    a.bias = bias;
+    a.add = add;
+    a.add_scale = add_scale;
+    a.act = (int32_t)act;
+    a.map = imap;
+    a.mask = mask;
+    a.perm = perm;
+    a.out = y;
+    a.status = status;
+    a.rows = n_out;
+    a.in_rows = n_in;
+    a.K = K;
+    a.cin = cin;
+    a.cout = cout;
+    a.wait_ns = wait_limit_ns();
+    return conv_i8(a, w, static_cast<cudaStream_t>(stream));
 }
 
 size_t spc_map_row_order_workspace_size(int64_t n) { return n < 0 ? 0 : row_order_ws_bytes(n); }
@@ -423,6 +497,8 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
         a.residual = nullptr;
         a.add_scale = 0.f;
         a.act = 0;
+        a.b_mn = 0;
+        a.wait_ns = wait_limit_ns();
         const spc_status s2 = conv_gather_tc(a, dt, st);
         if (s2 != SPC_ERR_UNSUPPORTED) return s2;
     }
@@ -478,6 +554,7 @@ spc_status spc_conv_wgrad(const void* x, const void* dy, const int32_t* imap, in
         t.splits = wgrad_tc_splits(K, n_out, cin, cout);
         t.chunk = ceil_div(ceil_div(n_out, t.splits), 128) * 128;
         t.splits = (int)ceil_div(n_out, t.chunk);
+        t.wait_ns = wait_limit_ns();
         spc_status s2 = wgrad_tc(t, dt, st);
         if (s2 == SPC_OK) return wgrad_reduce(t.part, K, cin, cout, t.splits, dw, st);
         if (s2 != SPC_ERR_UNSUPPORTED) return s2;

@@ -27,19 +27,22 @@
 // stored by their threads).  Every output row is written once: no atomics,
 // run-to-run identical.
 //
-// Forward: B = the weight slice transposed to [Cout][Cin] (K-major), prepared
-// once per call in the workspace.  dinput: rows are input rows, the map is the
-// transposed or mirrored map, and B = W[k] as stored ([Cin][Cout] is already
-// [N][K] K-major for that product).
+// Forward: B = W[k] as stored, [Cin][Cout], read as an MN-major operand (K =
+// Cin rows of N = Cout contiguous channels), loaded with 2-D TMA boxes of 64
+// rows x 64 channels; the 16- and 32-channel row shapes and tf32 take the
+// weights transposed to [Cout][Cin] (K-major) in the workspace instead.
+// dinput: rows are input rows, the map is the transposed or mirrored map, and
+// B = W[k] as stored ([Cin][Cout] is already [N][K] K-major for that product).
 //
-// Every barrier wait is bounded (2 s of wall time); a wait that runs out sets
-// SPC_ERR_TIMEOUT in the status word, the CTA waits (bounded) for the copies it
-// issued and for its MMAs, frees its tensor memory and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+// Every wait is bounded.  The waits of one warp role on another (a free stage,
+// a full stage) give up after the library's wait limit (spc_set_wait_limit_ns,
+// 2 s by default); a wait that runs out sets SPC_ERR_TIMEOUT in the status
+// word, and the CTA then waits for the copies and MMAs it issued itself (bounded
+// by 2 s: those always complete), frees its tensor memory and returns.
+#include "conv_tile.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace spc {
 
@@ -65,7 +68,7 @@ constexpr int kHalf = 128;  // rows per MMA (M)
 #ifndef TCN_STAGES
 #define TCN_STAGES 8
 #endif
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 2000000000ull;  // bound of the waits for a CTA's own copies / MMAs
 
 // MT 128-row MMA tiles per CTA share every weight stage (MT accumulators in
 // TMEM); NW warps gather rows and later run the epilogue; warp NW issues the
@@ -101,10 +104,13 @@ template <> struct TcKind<__half> { static constexpr int kind = 0; static conste
 template <> struct TcKind<__nv_bfloat16> { static constexpr int kind = 0; static constexpr uint32_t fmt = 1; };
 template <> struct TcKind<float> { static constexpr int kind = 1; static constexpr uint32_t fmt = 2; };
 
-template <typename T, int BN, int STAGES, int MT, int NW, int RB>
+// DENSE: K == 1 on the identity map (a per-voxel GEMM): the A tiles are whole
+// row blocks of the input, loaded with 2-D TMA like the weights (no gathers,
+// no map entries); the gather warps only run the epilogue.
+template <typename T, int BN, int STAGES, int MT, int NW, int RB, bool BMN, bool DENSE>
 __global__ void __launch_bounds__(TcShape<T, BN, STAGES, MT, NW, RB>::kThreads, TcShape<T, BN, STAGES, MT, NW, RB>::kMinCtas)
 k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ CUtensorMap tma_o,
-          int tstore)
+          const __grid_constant__ CUtensorMap tma_a, int tstore)
 {
     using S = TcShape<T, BN, STAGES, MT, NW, RB>;
     constexpr int kRowsPerCta = S::kRowsPerCta, kWorkers = S::kWorkers;
@@ -122,11 +128,11 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row0 = (int64_t)blockIdx.x * kRowsPerCta;
     const int n0 = blockIdx.y * BN;
-    const uint32_t kmask = K >= 32 ? 0xffffffffu : ((1u << K) - 1u);
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&full[s], kWorkers + 1);  // one copy completion per worker + the weight TMA
+            // one copy completion per worker + the weight TMA (dense: the TMA alone)
+            ptx::mbar_init(&full[s], DENSE ? 1 : kWorkers + 1);
             ptx::mbar_init(&empty[s], 1);
         }
         ptx::mbar_init(done, 1);
@@ -135,7 +141,10 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
         s_ctrl[2] = 0;
         ptx::mbar_init_fence();
     }
-    if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tma_b);
+    if (warp == kTmaWarp && lane == 0) {
+        ptx::prefetch_tmap(&tma_b);
+        if (DENSE) ptx::prefetch_tmap(&tma_a);
+    }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&s_ctrl[3]), S::TMEM_COLS);
         ptx::tmem_relinquish();
@@ -144,83 +153,15 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
     __syncthreads();
     ptx::tc_fence_after();
 
-    // union of the tile's row masks (thread t owns row t of the tile)
-    // tile row -> output row: the identity, or a caller's order that puts rows
-    // with the same offsets into the same tiles
-    const bool rvalid = tid < kRowsPerCta && row0 + tid < a.rows;
-    const int64_t row = rvalid && a.perm ? (int64_t)__ldg(a.perm + row0 + tid) : row0 + tid;
-    // Map entries of the tile's rows into s_idx, one row of s_idx per offset
-    // that some row of the tile uses.  Rows in a caller's grouped order have
-    // few offsets each: their masks are read first and only those entries are
-    // loaded.  Otherwise all K entries of a row are loaded in one burst (no
-    // dependent mask read first) and the tile's offsets are those where some
-    // row has an entry.
-    const bool by_mask = a.perm && a.mask;
-    int32_t iv[32];
-    uint32_t m = 0;
-    if (tid < kRowsPerCta) {
-        if (by_mask) {
-            if (rvalid) {
-                m = __ldcs(a.mask + row);  // read once: evict first
-                if (a.mirror) m = __brev(m) >> (32 - K);
-                m &= kmask;
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                iv[k] = -1;
-                if (k < K && rvalid) {
-                    const int mk = a.mirror ? K - 1 - k : k;
-                    iv[k] = a.map ? __ldcs(a.map + (int64_t)mk * a.rows + row) : (int32_t)row;
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                if (iv[k] >= a.in_rows || iv[k] < 0) iv[k] = -1;
-                m |= (iv[k] >= 0 ? 1u : 0u) << k;
-            }
-        }
-        const uint32_t wu = __reduce_or_sync(FULL_MASK, m);
-        if (lane == 0 && wu) atomicOr(reinterpret_cast<unsigned*>(&s_ctrl[2]), wu);
-    }
-    __syncthreads();
-    const uint32_t uni = (uint32_t)s_ctrl[2];
-    if (tid == 0) {
-        uint32_t u = uni;
-        int n = 0;
-        while (u) {
-            s_active[n++] = __ffs(u) - 1;
-            u &= u - 1;
-        }
-        s_ctrl[0] = n;
-    }
-    if (tid < kRowsPerCta && !by_mask) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-            if ((uni >> k) & 1u) s_idx[__popc(uni & ((1u << k) - 1u)) * kRowsPerCta + tid] = iv[k];
-    }
-    __syncthreads();
-    const int nact = s_ctrl[0];
-    if (by_mask) {
-        if (tid < kRowsPerCta) {
-            // this row's entries for the tile's active offsets, all loads in flight
-            // before the first store
-#pragma unroll
-            for (int ai = 0; ai < 32; ++ai) {
-                iv[ai] = -1;
-                if (ai < nact) {
-                    const int k = s_active[ai];
-                    if (rvalid && ((m >> k) & 1u)) {
-                        const int mk = a.mirror ? K - 1 - k : k;
-                        iv[ai] = __ldcs(a.map + (int64_t)mk * a.rows + row);
-                    }
-                }
-            }
-#pragma unroll
-            for (int ai = 0; ai < 32; ++ai)
-                if (ai < nact) s_idx[ai * kRowsPerCta + tid] = (iv[ai] >= 0 && iv[ai] < a.in_rows) ? iv[ai] : -1;
-        }
+    // the tile's map entries (thread t owns row t of the tile) and active offsets
+    int nact = 1;
+    if constexpr (DENSE) {
+        if (tid == 0) s_active[0] = 0;
         __syncthreads();
+    } else {
+        const TileMap tm{a.map, a.mask, a.perm, a.rows, a.in_rows, a.K, a.mirror};
+        nact = tile_map_entries<kRowsPerCta>(tm, row0, tid, s_idx, s_active, &s_ctrl[0],
+                                             reinterpret_cast<unsigned*>(&s_ctrl[2]));
     }
     const int kchunks = a.cred / S::CH;
     const int n_iter = nact * kchunks;
@@ -228,6 +169,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
 
     const uint8_t* in = static_cast<const uint8_t*>(a.in);
     if (tid < kWorkers) {
+        if constexpr (!DENSE) {
         // -------------------------------------------------- row-gather producers
         // A stage: the tile's rows x RB / 16 chunks of 16 bytes; chunk e = j *
         // kWorkers + tid, so a warp instruction copies whole row segments (four
@@ -240,7 +182,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % STAGES;
             bool ok = true;
-            if (it >= STAGES) ok = ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitNs);
+            if (it >= STAGES) ok = ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, a.wait_ns);
             if (!ok) {
                 atomicExch(&s_ctrl[1], 1);
                 break;
@@ -264,13 +206,14 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
             ptx::cp_async_arrive_noinc(&full[s]);
         }
         ptx::cp_async_wait_all();  // nothing of ours may still land when the CTA ends
+        }
     } else if (warp == kTmaWarp) {
         // -------------------------------------------------- weight producer (TMA)
         int issued = 0;
         if (lane == 0) {
             for (int it = 0; it < n_iter; ++it) {
                 const int s = it % STAGES;
-                if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, kWaitNs)) {
+                if (it >= STAGES && !ptx::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, a.wait_ns)) {
                     atomicExch(&s_ctrl[1], 1);
                     break;
                 }
@@ -278,21 +221,38 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
                 const int c0 = (it % kchunks) * S::CH;
                 const int k = s_active[ai];
                 const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
-                ptx::mbar_arrive_expect_tx(&full[s], S::B_BYTES);
-                ptx::tma_tile2d(a_base + S::A_BYTES, &tma_b, c0, k * a.n_total + n0, &full[s]);
+                ptx::mbar_arrive_expect_tx(&full[s], DENSE ? S::A_BYTES + S::B_BYTES : S::B_BYTES);
+                if constexpr (DENSE) {
+                    // the tile's own rows: MT boxes of 128 rows x RB bytes (rows past
+                    // the end read as zeros)
+#pragma unroll
+                    for (int h = 0; h < MT; ++h)
+                        ptx::tma_tile2d(a_base + h * kHalf * RB, &tma_a, c0, (int32_t)(row0 + h * kHalf),
+                                        &full[s]);
+                }
+                if constexpr (BMN) {
+                    // K = input channels c0.. of offset k (rows of W), N atoms of 64 channels
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        ptx::tma_tile2d(a_base + S::A_BYTES + j * (S::CH * 128), &tma_b, n0 + 64 * j,
+                                        k * a.cred + c0, &full[s]);
+                } else {
+                    ptx::tma_tile2d(a_base + S::A_BYTES, &tma_b, c0, k * a.n_total + n0, &full[s]);
+                }
                 ++issued;
             }
             // make sure no copy issued above is still landing before the CTA ends
             const int first = issued > STAGES ? issued - STAGES : 0;
             for (int it = first; it < issued; ++it)
-                ptx::mbar_wait(&full[it % STAGES], (it / STAGES) & 1, kWaitNs);
+                ptx::mbar_wait(&full[it % STAGES], (it / STAGES) & 1, kDrainNs);
         }
     } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------- MMA issuer
-        const uint32_t idesc = ptx::idesc_make(TcKind<T>::fmt, kHalf, BN);
+        // B MN-major (the forward's W[k] as stored): transpose bit of the descriptor
+        const uint32_t idesc = ptx::idesc_make(TcKind<T>::fmt, kHalf, BN) | (BMN ? 1u << 16 : 0u);
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % STAGES;
-            if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, kWaitNs)) {
+            if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, a.wait_ns)) {
                 atomicExch(&s_ctrl[1], 1);
                 break;
             }
@@ -301,7 +261,11 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_after();
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
-            const uint64_t bd = ptx::desc_k_sw<RB>(a_base + S::A_BYTES);
+            // K-major B advances 32 bytes along its rows per instruction; MN-major
+            // B advances two 8-row K groups (2048 bytes)
+            const uint64_t bd = BMN ? ptx::desc_mn_sw128(a_base + S::A_BYTES, S::CH * 128)
+                                    : ptx::desc_k_sw<RB>(a_base + S::A_BYTES);
+            constexpr uint64_t kBStep = BMN ? 2048 >> 4 : 2;
 #pragma unroll
             for (int kk = 0; kk < RB / 32; ++kk) {  // 32 bytes of K per instruction
                 const uint32_t acc = (it | kk) != 0 ? 1u : 0u;
@@ -309,7 +273,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
                 for (int h = 0; h < MT; ++h)
                     ptx::mma<TcKind<T>::kind>(tmem + h * BN,
                                               ptx::desc_k_sw<RB>(a_base + h * kHalf * RB) + 2 * kk,
-                                              bd + 2 * kk, idesc, acc);
+                                              bd + kBStep * kk, idesc, acc);
             }
             ptx::mma_commit(&empty[s]);
         }
@@ -318,7 +282,7 @@ k_conv_tc(TcArgs a, const __grid_constant__ CUtensorMap tma_b, const __grid_cons
 
     // ---------------------------------------------------------------- epilogue
     if (tid < kWorkers) {
-        const bool waited = ptx::mbar_wait(done, 0, kWaitNs);
+        const bool waited = ptx::mbar_wait(done, 0, kDrainNs);
         ptx::tc_fence_after();
         const bool aborted = __any_sync(FULL_MASK, !waited || s_ctrl[1] != 0);
         // warp w reads TMEM lanes 32*(w%4).. (its lane quarter) of accumulator
@@ -431,23 +395,6 @@ __global__ void __launch_bounds__(256) k_transpose_w(const T* __restrict__ w, T*
     }
 }
 
-using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
-
-// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
-EncodeFn encoder()
-{
-    static EncodeFn fn = []() -> EncodeFn {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeFn>(p);
-    }();
-    return fn;
-}
-
 template <typename T> struct TmaType;
 template <> struct TmaType<__half> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; };
 template <> struct TmaType<__nv_bfloat16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; };
@@ -457,26 +404,27 @@ template <> struct TmaType<float> { static constexpr CUtensorMapDataType v = CU_
 template <typename T, int RB>
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows)
 {
-    EncodeFn enc = encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * sizeof(T)};
-    const cuuint32_t box[2] = {(cuuint32_t)(RB / sizeof(T)), box_rows};
     const CUtensorMapSwizzle swz = RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : (RB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, TmaType<T>::v, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tmap_2d(m, TmaType<T>::v, (int)sizeof(T), base, cols, rows, (uint32_t)(RB / sizeof(T)),
+                   box_rows, swz);
 }
 
-template <typename T, int BN, int STAGES, int MT, int NW, int RB>
+template <typename T, int BN, int STAGES, int MT, int NW, int RB, bool BMN, bool DENSE = false>
 spc_status launch_tc(const TcArgs& a, cudaStream_t st)
 {
     using S = TcShape<T, BN, STAGES, MT, NW, RB>;
     static_assert(NW % (4 * MT) == 0 && (BN / (NW / (4 * MT))) % 16 == 0, "epilogue split");
+    static_assert(!BMN || (RB == 128 && sizeof(T) == 2 && BN % 64 == 0), "MN-major B shape");
     CUtensorMap tb;
-    if (!make_tmap<T, RB>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN))
+    // B as stored [K * cred rows][n_total] (boxes of 64 K rows x 64 channels), or
+    // transposed [K * n_total rows][cred] (boxes of BN rows x RB bytes)
+    const bool tb_ok = BMN ? make_tmap<T, 128>(&tb, a.b, (uint64_t)a.n_total, (uint64_t)a.K * a.cred, S::CH)
+                           : make_tmap<T, RB>(&tb, a.b, (uint64_t)a.cred, (uint64_t)a.K * a.n_total, BN);
+    if (!tb_ok) return SPC_ERR_UNSUPPORTED;
+    // dense A: the input [in_rows][cred] in boxes of 128 rows x RB bytes
+    CUtensorMap ta = tb;
+    if (DENSE && !make_tmap<T, RB>(&ta, a.in, (uint64_t)a.cred, (uint64_t)a.in_rows, kHalf))
         return SPC_ERR_UNSUPPORTED;
     // Output rows in tile order (no caller permutation) leave through TMA stores
     // when the output is a valid tensor-map target (16-byte aligned base).
@@ -490,7 +438,7 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
         }
     }
     const size_t smem = S::smem_bytes(a.K);
-    auto kern = k_conv_tc<T, BN, STAGES, MT, NW, RB>;
+    auto kern = k_conv_tc<T, BN, STAGES, MT, NW, RB, BMN, DENSE>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPC_ERR_CUDA;
@@ -501,7 +449,7 @@ spc_status launch_tc(const TcArgs& a, cudaStream_t st)
         configured[dev] = true;
     }
     dim3 grid((unsigned)ceil_div(a.rows, S::kRowsPerCta), (unsigned)(a.n_total / BN));
-    kern<<<grid, S::kThreads, smem, st>>>(a, tb, to, tstore);
+    kern<<<grid, S::kThreads, smem, st>>>(a, tb, to, ta, tstore);
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }
@@ -515,10 +463,36 @@ bool two_per_sm(int K)
     return 2 * (TcShape<T, BN, STAGES, MT, NW, RB>::smem_bytes(K) + kSmemPerCta) <= kSmemPerSm;
 }
 
+// 128-byte rows: B MN-major (W as stored) when the caller passes it so.
+template <typename T, int BN, int STAGES, int MT, int NW>
+spc_status launch_wide(const TcArgs& a, cudaStream_t st)
+{
+    if constexpr (sizeof(T) == 2) {
+        if (a.b_mn) return launch_tc<T, BN, STAGES, MT, NW, 128, true>(a, st);
+    }
+    return launch_tc<T, BN, STAGES, MT, NW, 128, false>(a, st);
+}
+
+// K == 1 on the identity map: TMA-loaded row blocks, two CTAs of 2 x 128 rows
+// per SM.
+template <typename T, int BN>
+spc_status launch_dense(const TcArgs& a, cudaStream_t st)
+{
+    if (a.b_mn) return launch_tc<T, BN, 2, 2, 8, 128, true, true>(a, st);
+    return launch_tc<T, BN, 2, 2, 8, 128, false, true>(a, st);
+}
+
 template <typename T>
 spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
 {
     constexpr int E = (int)sizeof(T);
+    if constexpr (E == 2) {
+        if (a.map == nullptr && a.K == 1 && a.perm == nullptr && a.cred % 64 == 0 &&
+            a.in_rows == a.rows) {
+            if (a.n_total % 128 == 0) return launch_dense<T, 128>(a, st);
+            if (a.n_total % 64 == 0) return launch_dense<T, 64>(a, st);
+        }
+    }
     if (a.cred * E % 128 == 0) {
         // Two CTAs per SM wherever the tile's shared memory allows: while one
         // CTA loads its map entries or stores its rows, the other's gathers keep
@@ -528,25 +502,26 @@ spc_status dispatch_tc(const TcArgs& a, cudaStream_t st)
         // stages.  One CTA of 2 x 128 rows, 16 warps and 4 stages is the shape
         // when neither fits.  Rows in grouped order run only a few offsets per
         // tile and take 128-row tiles.
-        if (a.perm && a.n_total % 128 == 0) return launch_tc<T, 128, 2, 1, 8, 128>(a, st);
-        if (a.perm) return launch_tc<T, 64, 2, 1, 8, 128>(a, st);
+        if (a.perm && a.n_total % 128 == 0) return launch_wide<T, 128, 2, 1, 8>(a, st);
+        if (a.perm) return launch_wide<T, 64, 2, 1, 8>(a, st);
         if (a.n_total % 128 == 0) {
-            if (two_per_sm<T, 128, 2, 2, 8, 128>(a.K)) return launch_tc<T, 128, 2, 2, 8, 128>(a, st);
-            if (two_per_sm<T, 128, 3, 1, 8, 128>(a.K)) return launch_tc<T, 128, 3, 1, 8, 128>(a, st);
-            return launch_tc<T, 128, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
+            if (two_per_sm<T, 128, 2, 2, 8, 128>(a.K)) return launch_wide<T, 128, 2, 2, 8>(a, st);
+            if (two_per_sm<T, 128, 3, 1, 8, 128>(a.K)) return launch_wide<T, 128, 3, 1, 8>(a, st);
+            return launch_wide<T, 128, TC_STAGES, TC_MT, TC_NW>(a, st);
         }
-        if (two_per_sm<T, 64, 2, 2, 8, 128>(a.K)) return launch_tc<T, 64, 2, 2, 8, 128>(a, st);
-        return launch_tc<T, 64, TC_STAGES, TC_MT, TC_NW, 128>(a, st);
+        if (two_per_sm<T, 64, 2, 2, 8, 128>(a.K)) return launch_wide<T, 64, 2, 2, 8>(a, st);
+        return launch_wide<T, 64, TC_STAGES, TC_MT, TC_NW>(a, st);
     }
-    // narrow rows (32 or 64 bytes): small stages, many CTAs per SM
+    // narrow rows (32 or 64 bytes): small stages, many CTAs per SM; B K-major
+    if (a.b_mn) return SPC_ERR_UNSUPPORTED;
     if (a.cred * E == 64) {
-        if (a.n_total == 16) return launch_tc<T, 16, TCN_STAGES, TCN_MT, TCN_NW, 64>(a, st);
-        if (a.n_total == 32) return launch_tc<T, 32, TCN_STAGES, TCN_MT, TCN_NW, 64>(a, st);
-        if (a.n_total % 64 == 0) return launch_tc<T, 64, TCN_STAGES, TCN_MT, TCN_NW, 64>(a, st);
+        if (a.n_total == 16) return launch_tc<T, 16, TCN_STAGES, TCN_MT, TCN_NW, 64, false>(a, st);
+        if (a.n_total == 32) return launch_tc<T, 32, TCN_STAGES, TCN_MT, TCN_NW, 64, false>(a, st);
+        if (a.n_total % 64 == 0) return launch_tc<T, 64, TCN_STAGES, TCN_MT, TCN_NW, 64, false>(a, st);
     } else if (a.cred * E == 32) {
-        if (a.n_total == 16) return launch_tc<T, 16, TCN_STAGES, TCN_MT, TCN_NW, 32>(a, st);
-        if (a.n_total == 32) return launch_tc<T, 32, TCN_STAGES, TCN_MT, TCN_NW, 32>(a, st);
-        if (a.n_total % 64 == 0) return launch_tc<T, 64, TCN_STAGES, TCN_MT, TCN_NW, 32>(a, st);
+        if (a.n_total == 16) return launch_tc<T, 16, TCN_STAGES, TCN_MT, TCN_NW, 32, false>(a, st);
+        if (a.n_total == 32) return launch_tc<T, 32, TCN_STAGES, TCN_MT, TCN_NW, 32, false>(a, st);
+        if (a.n_total % 64 == 0) return launch_tc<T, 64, TCN_STAGES, TCN_MT, TCN_NW, 32, false>(a, st);
     }
     return SPC_ERR_UNSUPPORTED;
 }
@@ -564,6 +539,11 @@ bool conv_tc_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt, spc_
     }
     if (dt == SPC_F32) return prec == SPC_PREC_TF32 && cred % 32 == 0 && wide_n;
     return false;
+}
+
+bool conv_tc_reads_w_as_stored(int32_t cin, int32_t cout, spc_dtype dt)
+{
+    return (dt == SPC_F16 || dt == SPC_BF16) && cin % 64 == 0 && cout % 64 == 0;
 }
 
 size_t conv_tc_weight_bytes(int32_t K, int32_t cin, int32_t cout, spc_dtype dt)

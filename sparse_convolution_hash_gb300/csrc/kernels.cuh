@@ -7,6 +7,10 @@
 
 namespace spc {
 
+// Bound (ns) of the waits of one warp role on another in the pipelined
+// tensor-core kernels, as set by spc_set_wait_limit_ns (api.cu).
+uint64_t wait_limit_ns();
+
 // ------------------------------------------------------------------ hash table
 // Open addressing over 32-byte buckets of four 64-bit slots.  A slot holds
 // (cell key << vbits) | row, or all ones when empty.  A 4-lane group of a warp
@@ -125,7 +129,10 @@ bool conv_narrow_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt);
 spc_status conv_gather_narrow(const GatherGemm& p, spc_dtype dt, cudaStream_t st);
 
 // Tensor-core gathered GEMM (tcgen05): out[r, n] = bias[n] + sum_k sum_c
-// in[map(k, r), c] * b[k][n][c], with b already in [K][n_total][cred] order.
+// in[map(k, r), c] * B(k, c, n), with B(k, c, n) = b[k][n][c] (b in
+// [K][n_total][cred] order), or b[k][c][n] when b_mn (weights as stored; 16-bit
+// types with cred and n_total multiples of 64 only).  wait_ns bounds the waits
+// of one warp role on another (SPC_ERR_TIMEOUT when one runs out).
 struct TcArgs {
     const void* in;
     const void* b;
@@ -140,12 +147,40 @@ struct TcArgs {
     float add_scale;
     int32_t act;
     const int32_t* perm;    // tile row r computes output row perm[r] (NULL: r)
+    int32_t b_mn;
+    uint64_t wait_ns;
 };
 bool conv_tc_supported(int32_t cred, int32_t cout, int32_t K, spc_dtype dt, spc_precision prec);
+// True when the forward reads W as stored (no transposed copy in the workspace).
+bool conv_tc_reads_w_as_stored(int32_t cin, int32_t cout, spc_dtype dt);
 size_t conv_tc_weight_bytes(int32_t K, int32_t cin, int32_t cout, spc_dtype dt);
 spc_status transpose_weights(const void* w, void* wt, int32_t K, int32_t cin, int32_t cout,
                              spc_dtype dt, cudaStream_t st);
 spc_status conv_gather_tc(const TcArgs& a, spc_dtype dt, cudaStream_t st);
+
+// Quantized forward (conv_i8.cu): int8 codes in and out, exact integer sums on
+// the fp16 tensor-core path, per-channel fp32 scale and bias, optional int8
+// residual add and ReLU.  wq is the workspace for the split weights.
+struct I8Args {
+    const int8_t* in;
+    __half* wq;
+    const float* scale;
+    const float* bias;      // or NULL
+    const int8_t* add;      // [rows, cout] or NULL
+    float add_scale;
+    int32_t act;
+    const int32_t* map;
+    const uint32_t* mask;
+    const int32_t* perm;    // tile row r computes output row perm[r] (NULL: r)
+    int8_t* out;
+    int32_t* status;
+    int64_t rows, in_rows;
+    int32_t K, cin, cout;
+    uint64_t wait_ns;
+};
+bool conv_i8_supported(int32_t K, int32_t cin, int32_t cout);
+size_t conv_i8_ws_bytes(int32_t K, int32_t cin, int32_t cout);
+spc_status conv_i8(const I8Args& a, const int8_t* w, cudaStream_t st);
 
 // dW[k] = sum_o x[map[k,o]]^T dy[o] in fp32, deterministic split over output rows.
 struct WgradArgs {
@@ -171,6 +206,7 @@ struct WgradTcArgs {
     int64_t n_in, n_out;
     int64_t chunk;          // output rows per split (multiple of 128)
     int32_t K, cin, cout, splits;
+    uint64_t wait_ns;       // bound of the waits of one warp role on another
 };
 bool wgrad_tc_supported(int32_t K, int32_t cin, int32_t cout, spc_dtype dt);
 int wgrad_tc_splits(int32_t K, int64_t n_out, int32_t cin, int32_t cout);

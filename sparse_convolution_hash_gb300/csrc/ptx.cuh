@@ -45,19 +45,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
 // try_wait that may suspend the thread in hardware for up to `hint_ns` while
 // the phase is incomplete (it resumes as soon as the phase completes).
 __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns)
@@ -73,11 +60,42 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
     return done != 0;
 }
 
-// Waits for the phase with the given parity to complete; gives up after
-// `limit_ns` nanoseconds of wall time and returns false.  Waiting threads are
-// suspended in hardware between polls instead of spinning on issue slots.
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// try_wait without a time hint: may suspend the thread for a system-dependent
+// time while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase with the given parity to complete; gives up once
+// `limit_ns` nanoseconds of wall time have passed and returns false.  A limit
+// of 0 only tests the phase (no wait at all).  Waiting threads are suspended in
+// hardware between polls instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
 {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
@@ -298,6 +316,21 @@ __device__ __forceinline__ uint64_t desc_k_sw(uint32_t saddr)
     d |= (uint64_t)((8 * RB) >> 4) << 32;           // stride byte offset: 8 rows
     d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
     d |= layout << 61;                              // swizzle mode
+    return d;
+}
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle
+// layout: atoms of 8 reduction (K) rows x 128 bytes (64 16-bit elements of M
+// or N); K groups of 8 rows every 1024 bytes (stride byte offset), and
+// successive 64-element MN atoms `lbo` bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t lbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);        // start address
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;     // leading byte offset: next MN atom
+    d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: next 8 K rows
+    d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                         // layout: 128-byte swizzle
     return d;
 }
 

@@ -14,14 +14,13 @@
 // CTA writes its partial tiles to the workspace; k_wgrad_reduce sums the
 // chunks in a fixed order, so dW is run-to-run bit-identical.
 //
-// Every barrier wait is bounded (2 s); a wait that runs out sets
-// SPC_ERR_TIMEOUT, the CTA waits (bounded) for its copies and MMAs, frees its
-// tensor memory and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+// Every wait is bounded.  The waits of one warp role on another give up after
+// the library's wait limit (spc_set_wait_limit_ns, 2 s by default) and set
+// SPC_ERR_TIMEOUT; the CTA then waits for the copies and MMAs it issued itself
+// (bounded by 2 s: those always complete), frees its tensor memory and returns.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace spc {
 
@@ -33,7 +32,7 @@ constexpr int kStages = 4;      // x-gather stages (a power of two)
 constexpr int kWorkers = 256;   // warps 0-7: gathers (four 16-byte copies each per stage); warps 0-3 then run the epilogue
 constexpr int kThreads = kWorkers + 64;  // warp 16: dy TMA; warp 17: TMEM owner, MMA issuer
 constexpr int kTmaWarp = kWorkers / 32, kMmaWarp = kTmaWarp + 1;
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 2000000000ull;  // bound of the waits for a CTA's own copies / MMAs
 constexpr int kABytes = kRows * 128;  // 64 channels x 2 bytes per row
 constexpr int kBBytes = kRows * 128;
 
@@ -46,19 +45,6 @@ size_t smem_bytes()
 {
     const size_t need = 1024 + (size_t)kStages * kABytes + 2 * (size_t)kBBytes + 8 * (2 * kStages + 5) + 64;
     return need;
-}
-
-// MN-major operand, 128-byte swizzle: 8 reduction rows of 128 bytes per atom,
-// atoms stacked every 1024 bytes (stride byte offset).
-__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-    d |= (uint64_t)1 << 16;            // leading byte offset: unused (one atom wide)
-    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8 reduction rows
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
 }
 
 template <typename T>
@@ -151,7 +137,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
                 if (g >= ng) break;
                 const int it = rc * ng + g;
                 const int s = it % kStages;
-                if (it >= kStages && !ptx::mbar_wait(&aempty[s], ((it / kStages) - 1) & 1, kWaitNs)) {
+                if (it >= kStages && !ptx::mbar_wait(&aempty[s], ((it / kStages) - 1) & 1, a.wait_ns)) {
                     atomicExch(&s_ctrl[0], 1);
                     ok = false;
                     break;
@@ -179,7 +165,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
             int issued = 0;
             for (int rc = 0; rc < nrc; ++rc) {
                 const int b = rc & 1;
-                if (rc >= 2 && !ptx::mbar_wait(&bempty[b], ((rc >> 1) - 1) & 1, kWaitNs)) {
+                if (rc >= 2 && !ptx::mbar_wait(&bempty[b], ((rc >> 1) - 1) & 1, a.wait_ns)) {
                     atomicExch(&s_ctrl[0], 1);
                     break;
                 }
@@ -189,7 +175,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
                 ++issued;
             }
             const int first = issued > 2 ? issued - 2 : 0;
-            for (int rc = first; rc < issued; ++rc) ptx::mbar_wait(&bfull[rc & 1], (rc >> 1) & 1, kWaitNs);
+            for (int rc = first; rc < issued; ++rc) ptx::mbar_wait(&bfull[rc & 1], (rc >> 1) & 1, kDrainNs);
         }
     } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------- MMA issuer
@@ -200,7 +186,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
         bool ok = true;
         for (int rc = 0; rc < nrc && ok; ++rc) {
             const int b = rc & 1;
-            if (!ptx::mbar_wait(&bfull[b], (rc >> 1) & 1, kWaitNs)) {
+            if (!ptx::mbar_wait(&bfull[b], (rc >> 1) & 1, a.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -208,7 +194,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
             for (int g = 0; g < ng; ++g) {
                 const int it = rc * ng + g;
                 const int s = it % kStages;
-                if (!ptx::mbar_wait(&afull[s], (it / kStages) & 1, kWaitNs)) {
+                if (!ptx::mbar_wait(&afull[s], (it / kStages) & 1, a.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -217,8 +203,9 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
                 const uint32_t abase = ptx::smem_u32(As + (size_t)s * kABytes);
 #pragma unroll
                 for (int kk = 0; kk < kRows / 16; ++kk)  // 16 reduction rows (two atoms) per instruction
-                    ptx::mma<0>(tmem + (uint32_t)(g * 64), desc_mn_sw128(abase + kk * 2048),
-                                desc_mn_sw128(bbase + kk * 2048), idesc,
+                    // both operands one 64-element MN atom wide (leading byte offset unused)
+                    ptx::mma<0>(tmem + (uint32_t)(g * 64), ptx::desc_mn_sw128(abase + kk * 2048, 16),
+                                ptx::desc_mn_sw128(bbase + kk * 2048, 16), idesc,
                                 (rc | kk) != 0 ? 1u : 0u);
                 ptx::mma_commit(&aempty[s]);
             }
@@ -232,7 +219,7 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     // M = 64 accumulator rows sit in TMEM lanes 32 q + r (q < 4, r < 16): warp q
     // of the first four holds rows 16 q .. 16 q + 15 in its lanes 0-15.
     if (warp < 4) {
-        const bool waited = ptx::mbar_wait(done, 0, kWaitNs);
+        const bool waited = ptx::mbar_wait(done, 0, kDrainNs);
         ptx::tc_fence_after();
         const bool aborted = __any_sync(FULL_MASK, !waited || s_ctrl[0] != 0);
         if (aborted) {
@@ -272,37 +259,14 @@ k_wgrad_tc(WgradTcArgs a, const __grid_constant__ CUtensorMap tma_dy)
     }
 }
 
-using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
-
-EncodeFn encoder()
-{
-    static EncodeFn fn = []() -> EncodeFn {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeFn>(p);
-    }();
-    return fn;
-}
-
 template <typename T>
 spc_status launch(const WgradTcArgs& a, cudaStream_t st)
 {
-    EncodeFn enc = encoder();
-    if (!enc) return SPC_ERR_UNSUPPORTED;
     CUtensorMap tdy;
-    const cuuint64_t dims[2] = {(cuuint64_t)a.cout, (cuuint64_t)a.n_out};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.cout * sizeof(T)};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kRows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dtt = sizeof(T) == 2 && TcKindW<T>::fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (enc(&tdy, dtt, 2, const_cast<void*>(a.dy), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const CUtensorMapDataType dtt = TcKindW<T>::fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!tmap_2d(&tdy, dtt, 2, a.dy, (uint64_t)a.cout, (uint64_t)a.n_out, 64, kRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
         return SPC_ERR_UNSUPPORTED;
     static bool configured[64] = {};
     int dev = 0;

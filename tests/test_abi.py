@@ -152,10 +152,14 @@ def test_argument_errors_return_before_any_work(L):
     assert L.spc_map_row_order(ctypes.c_void_p(256), 27, 4, None, ctypes.c_void_p(256),
                                ctypes.c_void_p(256), 8, None) == 8
     assert L.spc_map_row_order_workspace_size(1000) >= 16 * 1000
-    # the tensor-core path needs its workspace (transposed weights)
-    assert L.spc_conv_workspace_size(27, 4, 4, 128, 128, binding.SPC_BF16) == 27 * 128 * 128 * 2
+    # 16-bit rows of multiples of 64 channels read W as stored: no workspace;
+    # the 32-channel rows take a transposed copy (as does tf32), which the
+    # tensor-core path requires
+    assert L.spc_conv_workspace_size(27, 4, 4, 128, 128, binding.SPC_BF16) == 0
+    assert L.spc_conv_workspace_size(27, 4, 4, 32, 128, binding.SPC_BF16) == 27 * 32 * 128 * 2
+    assert L.spc_conv_workspace_size(27, 4, 4, 64, 64, binding.SPC_F32) == 27 * 64 * 64 * 4
     assert L.spc_conv_fwd(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256),
-                          None, 27, 4, 4, 128, 128, binding.SPC_BF16, 0, ctypes.c_void_p(256),
+                          None, 27, 4, 4, 32, 128, binding.SPC_BF16, 0, ctypes.c_void_p(256),
                           None, None, 0, None) == 8
     assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
                             binding.SPC_MAP_SUBM_MIRROR, None, 27, 4, 5, 8, 8, 0, 0,
@@ -202,3 +206,39 @@ def test_noalloc_context_cache_logic(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, out.stderr
     assert "ctx cache ok" in out.stdout
+
+
+def test_wait_limit_setting(L):
+    old = binding.spc_get_wait_limit_ns()
+    assert old == 2_000_000_000
+    try:
+        binding.spc_set_wait_limit_ns(12345)
+        assert binding.spc_get_wait_limit_ns() == 12345
+        with pytest.raises(binding.SpcError):
+            binding.spc_set_wait_limit_ns(61_000_000_000)
+        assert binding.spc_get_wait_limit_ns() == 12345
+    finally:
+        binding.spc_set_wait_limit_ns(old)
+    assert binding.spc_get_wait_limit_ns() == old
+
+
+def test_int8_host_checks(L):
+    """The quantized forward's argument checks and workspace size (no launch)."""
+    P = ctypes.c_void_p
+    f = L.spc_conv_fwd_int8
+    assert L.spc_conv_int8_workspace_size(27, 128, 128) == 27 * 2 * 128 * 128 * 2
+    # K * cin beyond the exact range, or channels not multiples of 64: unsupported, size 0
+    assert L.spc_conv_int8_workspace_size(27, 320, 64) == 0
+    assert L.spc_conv_int8_workspace_size(27, 48, 64) == 0
+    args = lambda **o: [o.get("x", P(256)), o.get("w", P(256)), o.get("scale", P(256)), None,
+                        P(256), None, None, o.get("K", 27), 4, 4, o.get("cin", 64),
+                        o.get("cout", 64), o.get("add"), 1.0, o.get("act", 0), o.get("y", P(512)),
+                        None, o.get("ws", None), o.get("wsb", 0), None]
+    assert f(*args(scale=None)) == 1          # scale required
+    assert f(*args(w=P(258))) == 1            # misaligned weights
+    assert f(*args(act=2)) == 1               # unknown activation
+    assert f(*args(add=P(512))) == 1          # residual aliasing the output
+    assert f(*args(cin=320)) == 6             # K * cin > 8192
+    assert f(*args(cout=96)) == 6             # cout not a multiple of 64
+    assert f(*args()) == 8                    # workspace missing
+    assert f(*args(ws=P(256), wsb=1024)) == 8  # workspace too small

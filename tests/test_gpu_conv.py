@@ -349,3 +349,82 @@ def test_empty_conv():
     assert spc.spc_conv_fwd(x, w, None, imap).shape == (0, 16)
     dw = spc.spc_conv_wgrad(x, torch.zeros((0, 16), dtype=torch.bfloat16, device=d), imap, 27)
     assert (dw == 0).all()
+
+
+def test_dfilter_whole_offsets_shell192x4():
+    """Every dW entry of three whole offsets (a corner, a face and the centre) on
+    the full 4 x 192^3 training workload, where the split-row reduction is
+    longest: against the oracle's per-entry sums, normwise per offset."""
+    w = scenes.workload("shell192x4_train_bf16")
+    c = w["coords"]
+    d = dev()
+    m = spc.spc_build_indice_map(torch.from_numpy(c).to(d), 4, (192, 192, 192))
+    spc.check_status(m["status"])
+    imap_ref, _ = oracle.subm_map(c, 4, (192, 192, 192))
+    dw = to_np(spc.spc_conv_wgrad(w["x"].to(d), w["dy"].to(d), m["imap"], 27))
+    cin, cout = w["cin"], w["cout"]
+    for k in (0, 4, 13):
+        ent = k * cin * cout + np.arange(cin * cout)
+        ref = oracle.conv_wgrad_entries(w["x"], w["dy"], imap_ref, ent)
+        assert normwise(dw.reshape(-1)[ent], ref) < 2e-2, k
+
+
+def test_wait_limit_runs_out_with_a_status_and_the_context_survives():
+    """With the wait limit at 0 the pipelined tensor-core kernels give up at the
+    first stage handoff that is not already complete: the call's status word
+    reads SPC_ERR_TIMEOUT and the kernels return (no hang, no fault).  With the
+    limit restored the same context computes correct results."""
+    g = np.random.default_rng(5)
+    batch, shape = 2, (12, 11, 13)
+    coords = rand_coords(g, 3000, batch, shape)
+    x, w, b, dy, m, imap_ref = subm_case(coords, batch, shape, 64, 64, "bf16", seed=5, bias=False)
+    d = dev()
+    xd, wd, dyd = x.to(d), w.to(d), dy.to(d)
+    old = spc.binding.spc_get_wait_limit_ns()
+    assert old == 2_000_000_000
+    timeouts = {"fwd": 0, "dgrad": 0, "wgrad": 0}
+    try:
+        spc.binding.spc_set_wait_limit_ns(0)
+        for _ in range(3):
+            for what in timeouts:
+                st = spc.new_status(d)
+                if what == "fwd":
+                    spc.spc_conv_fwd(xd, wd, None, m["imap"], m["mask"], status=st)
+                elif what == "dgrad":
+                    spc.spc_conv_dgrad(dyd, wd, m["imap"], spc.SPC_MAP_SUBM_MIRROR, coords.shape[0],
+                                       mask=m["mask"], status=st)
+                else:
+                    spc.spc_conv_wgrad(xd, dyd, m["imap"], 27, status=st)
+                torch.cuda.synchronize()
+                code = int(st.item())
+                assert code in (0, 9), code  # SPC_OK or SPC_ERR_TIMEOUT
+                timeouts[what] += code == 9
+    finally:
+        spc.binding.spc_set_wait_limit_ns(old)
+    assert all(v > 0 for v in timeouts.values()), timeouts
+    st = spc.new_status(d)
+    y = spc.spc_conv_fwd(xd, wd, None, m["imap"], m["mask"], status=st)
+    dw = spc.spc_conv_wgrad(xd, dyd, m["imap"], 27, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, None, imap_ref)) < 2e-2
+    assert normwise(to_np(dw), oracle.conv_wgrad(x, dy, imap_ref)) < 2e-2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("n,cin,cout", [(1, 64, 64), (129, 128, 128), (1000, 64, 192),
+                                        (3001, 128, 64), (700, 192, 128)])
+def test_k1_dense_rows(dtype, n, cin, cout):
+    """K = 1 on the identity map (no map): the tensor-core kernel loads whole row
+    blocks with TMA; forward and dinput against the oracle, ragged tails included."""
+    g = np.random.default_rng(n + cin + cout)
+    x = rand_tensor(g, (n, cin), dtype)
+    w = rand_tensor(g, (1, cin, cout), dtype, std=float(np.sqrt(1.0 / cin)))
+    b = rand_tensor(g, (cout,), dtype, std=0.1)
+    dy = rand_tensor(g, (n, cout), dtype)
+    ident = np.arange(n, dtype=np.int32)[None, :]
+    d = dev()
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), None, n_out=n)
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, ident)) < TOL[(dtype, "exact")]
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), None, spc.SPC_MAP_SUBM_MIRROR, n)
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, ident, n)) < TOL[(dtype, "exact")]

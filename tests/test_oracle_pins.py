@@ -569,3 +569,24 @@ def test_int8_residual_relu_translation():
     imap2, _ = oracle.subm_map(shifted, 2, (8, 9, 10))
     y2, acc2 = oracle.conv_fwd_int8(x, w, sc, None, imap2, add=add, add_scale=0.5, relu=True)
     assert np.array_equal(y, y2) and np.array_equal(acc, acc2)
+
+
+def test_oracle_threads_do_not_change_results():
+    """The oracle's parallel row loops give the same bits at any thread count."""
+    coords, imap, x, w, g = _int8_case(15, n=400, cin=8, cout=6)
+    xf = g.standard_normal((400, 8))
+    wf = g.standard_normal((27, 8, 6))
+    shape, batch = (7, 8, 9), 2
+    try:
+        oracle.set_threads(1)
+        m1, c1 = oracle.subm_map(coords, batch, shape)
+        y1 = oracle.conv_fwd(xf, wf, None, m1)
+        q1, a1 = oracle.conv_fwd_int8(x, w, np.full(6, 0.01, np.float32), None, m1)
+        oracle.set_threads(4)
+        m4, c4 = oracle.subm_map(coords, batch, shape)
+        y4 = oracle.conv_fwd(xf, wf, None, m4)
+        q4, a4 = oracle.conv_fwd_int8(x, w, np.full(6, 0.01, np.float32), None, m4)
+    finally:
+        oracle.set_threads(1)
+    assert np.array_equal(m1, m4) and np.array_equal(c1, c4)
+    assert np.array_equal(y1, y4) and np.array_equal(q1, q4) and np.array_equal(a1, a4)
