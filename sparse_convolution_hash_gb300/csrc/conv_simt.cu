@@ -192,9 +192,55 @@ k_wgrad_partial(WgradArgs a, int ctiles, int jtiles, int splits, int64_t chunk,
         for (int r = 0; r < 4; ++r) dst[(tr * 4 + q) * WT + tc * 4 + r] = acc[q][r];
 }
 
+// dw[k][c][j] = sum over q = 0, 1, .. splits - 1 (in that order) of the partial
+// tiles part[(k, c / WT, j / WT)][q][c % WT][j % WT].  A thread owns four
+// consecutive j (one 16-byte load per partial) and keeps eight partial loads in
+// flight ahead of its in-order adds, so the result bits do not depend on the
+// launch shape.
 __global__ void __launch_bounds__(kThreads)
 k_wgrad_reduce(const float* __restrict__ part, int K, int cin, int cout, int ctiles, int jtiles,
                int splits, float* __restrict__ dw)
+{
+    const int64_t total4 = (int64_t)K * cin * cout / 4;  // cout % 4 == 0
+    for (int64_t e4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e4 < total4;
+         e4 += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = e4 * 4;
+        const int j = (int)(e % cout);
+        const int c = (int)((e / cout) % cin);
+        const int k = (int)(e / ((int64_t)cout * cin));
+        const int tile = (k * ctiles + c / WT) * jtiles + j / WT;
+        const float4* src = reinterpret_cast<const float4*>(part + (size_t)tile * splits * (WT * WT) +
+                                                            (c % WT) * WT + (j % WT));
+        constexpr int kStep = WT * WT / 4;  // float4s between successive partials
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        int q = 0;
+        for (; q + 8 <= splits; q += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcs(src + (size_t)(q + u) * kStep);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                s.x += v[u].x;
+                s.y += v[u].y;
+                s.z += v[u].z;
+                s.w += v[u].w;
+            }
+        }
+        for (; q < splits; ++q) {
+            const float4 v = __ldcs(src + (size_t)q * kStep);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        *reinterpret_cast<float4*>(dw + e) = s;
+    }
+}
+
+// The same sums one element per thread (any cout).
+__global__ void __launch_bounds__(kThreads)
+k_wgrad_reduce1(const float* __restrict__ part, int K, int cin, int cout, int ctiles, int jtiles,
+                int splits, float* __restrict__ dw)
 {
     const int64_t total = (int64_t)K * cin * cout;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
@@ -229,12 +275,7 @@ spc_status launch_wgrad(const WgradArgs& a, void* ws, cudaStream_t st)
     dim3 grid((unsigned)(a.K * ctiles * jtiles), (unsigned)splits);
     k_wgrad_partial<T><<<grid, kThreads, 0, st>>>(a, ctiles, jtiles, splits, chunk, part);
     SPC_LAUNCH_CHECK();
-    const int64_t total = (int64_t)a.K * a.cin * a.cout;
-    const int rgrid = (int)std::min<int64_t>(ceil_div(total, kThreads), 4 * sm_count());
-    k_wgrad_reduce<<<rgrid, kThreads, 0, st>>>(part, a.K, a.cin, a.cout, ctiles, jtiles, splits,
-                                               a.dw);
-    SPC_LAUNCH_CHECK();
-    return SPC_OK;
+    return wgrad_reduce(part, a.K, a.cin, a.cout, splits, a.dw, st);
 }
 
 }  // namespace
@@ -262,8 +303,14 @@ spc_status wgrad_reduce(const float* part, int32_t K, int32_t cin, int32_t cout,
     const int ctiles = (int)ceil_div(cin, WT), jtiles = (int)ceil_div(cout, WT);
     const int64_t total = (int64_t)K * cin * cout;
     if (total == 0) return SPC_OK;
-    const int rgrid = (int)std::min<int64_t>(ceil_div(total, kThreads), 4 * sm_count());
-    k_wgrad_reduce<<<rgrid, kThreads, 0, st>>>(part, K, cin, cout, ctiles, jtiles, splits, dw);
+    if (cout % 4 == 0 && (reinterpret_cast<uintptr_t>(dw) & 15u) == 0 &&
+        (reinterpret_cast<uintptr_t>(part) & 15u) == 0) {
+        const int rgrid = (int)std::min<int64_t>(ceil_div(total / 4, kThreads), 4 * sm_count());
+        k_wgrad_reduce<<<rgrid, kThreads, 0, st>>>(part, K, cin, cout, ctiles, jtiles, splits, dw);
+    } else {
+        const int rgrid = (int)std::min<int64_t>(ceil_div(total, kThreads), 4 * sm_count());
+        k_wgrad_reduce1<<<rgrid, kThreads, 0, st>>>(part, K, cin, cout, ctiles, jtiles, splits, dw);
+    }
     SPC_LAUNCH_CHECK();
     return SPC_OK;
 }
