@@ -75,6 +75,7 @@ DESCRIPTIONS = {
                      "bias, ReLU, int8 out), 256^3 shell, int8 128->128",
 }
 ELEM = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
+ROW_ORDER = [False]  # --row-order on: wide-channel submanifold tiles in mask-grouped row order
 
 
 def peaks():
@@ -224,16 +225,37 @@ class Case:
                 torch.cuda.synchronize()
                 B.check_status(self.status, "setup build")
                 self.pairs = int(self.m["pair_count"].sum().item())
+                # wide channels: the build also groups the rows by offset mask (one
+                # row order serves the forward, the dinput and the int8 forward)
+                self.grouped = ROW_ORDER[0] and cin >= 64 and cout >= 64
+                if self.grouped:
+                    nro = int(B.lib().spc_map_row_order_workspace_size(n))
+                    self.ro_ws = torch.empty(max(nro, 256), dtype=torch.uint8, device=dev)
+                    self.perm = torch.empty(n, dtype=torch.int32, device=dev)
+
+                def build():
+                    spc.spc_build_indice_map(self.coords, self.batch, self.shape, ksize=self.ks,
+                                             subm=True, out=self.m)
+                    if self.grouped:
+                        spc.spc_map_row_order(None, ws=self.ro_ws, mask=self.m["mask"], K=K,
+                                              perm=self.perm)
+
+                build()
+                torch.cuda.synchronize()
+                passes = (K + 7) // 8
                 self.phases.append(Phase(
-                    "build", lambda: spc.spc_build_indice_map(
-                        self.coords, self.batch, self.shape, ksize=self.ks, subm=True, out=self.m),
-                    "build", 16 * n + 4 * K * n + 4 * n + 4 * K,
-                    kernels="k_build_init, k_hash_insert, k_map_probe", launches=3))
+                    "build", build, "build", 16 * n + 4 * K * n + 4 * n + 4 * K + (4 * n if self.grouped else 0),
+                    kernels="k_build_init, k_hash_insert, k_map_probe" + (
+                        ", row order: k_row_keys_from_mask, k_radix_hist/k_scan_exclusive/k_radix_scatter "
+                        f"x{passes}, k_perm_from_keys" if self.grouped else ""),
+                    launches=3 + (2 + 3 * passes if self.grouped else 0)))
             else:
                 self.m = None
                 imap = mask = None
                 self.pairs = n
+                self.grouped = False
         else:
+            self.grouped = False
             st, pd = w["stride"], w["pad"]
             g = B.make_geom(self.ks, st, pd, 1)
             cap = n * K
@@ -295,9 +317,9 @@ class Case:
             self.conv_ws = torch.empty(max(nbw, 256), dtype=torch.uint8, device=dev)
             self.phases.append(Phase(
                 "fwd", lambda: spc.spc_conv_fwd_int8(self.x, self.wt, self.scale, self.qbias,
-                                                     self.imap, self.mask, act=B.SPC_ACT_RELU,
-                                                     out=self.y, status=self.status,
-                                                     ws=self.conv_ws),
+                                                     self.imap, self.mask, perm=self.perm_or_none(),
+                                                     act=B.SPC_ACT_RELU, out=self.y,
+                                                     status=self.status, ws=self.conv_ws),
                 "conv", n * cin + n_out * cout + K * cin * cout + 4 * P + 8 * cout,
                 2.0 * P * cin * cout, kernels="k_i8_split_w + k_conv_i8 (tcgen05, fp16 halves)",
                 launches=2))
@@ -357,7 +379,7 @@ class Case:
                 "fwd", lambda: spc.spc_conv_fwd_fused(
                     self.x, self.wt, self.bias, self.imap, self.mask, residual=self.x,
                     add_scale=1.0, act=B.SPC_ACT_RELU, n_out=n_out, precision=self.prec,
-                    out=self.y, status=self.status, ws=self.conv_ws),
+                    out=self.y, status=self.status, ws=self.conv_ws, perm=self.perm_or_none()),
                 "conv", s * n * cin + 2 * s * n_out * cout + s * K * cin * cout + 4 * P + bias_b,
                 flops, kernels=self.fwd_kernel() + ", fused residual + ReLU epilogue",
                 launches=2 if "tcgen05" in self.fwd_kernel() else 1))
@@ -365,7 +387,8 @@ class Case:
             self.phases.append(Phase(
                 "fwd", lambda: spc.spc_conv_fwd(self.x, self.wt, self.bias, self.imap, self.mask,
                                                 n_out=n_out, precision=self.prec, out=self.y,
-                                                status=self.status, ws=self.conv_ws),
+                                                status=self.status, ws=self.conv_ws,
+                                                perm=self.perm_or_none()),
                 "conv", s * n * cin + s * n_out * cout + s * K * cin * cout + 4 * P + bias_b, flops,
                 kernels=self.fwd_kernel(), launches=2 if "tcgen05" in self.fwd_kernel() else 1))
         self.train = bool(w.get("train"))
@@ -379,7 +402,8 @@ class Case:
             self.phases.append(Phase(
                 "dgrad", lambda: spc.spc_conv_dgrad(self.dy, self.wt, self.imap,
                                                     B.SPC_MAP_SUBM_MIRROR, n, mask=self.mask,
-                                                    out=self.dx, status=self.status),
+                                                    out=self.dx, status=self.status,
+                                                    perm=self.perm_or_none()),
                 "conv", s * n_out * cout + s * n * cin + s * K * cin * cout + 4 * P, flops,
                 kernels=self.fwd_kernel(dgrad=True)))
             self.phases.append(Phase(
@@ -389,6 +413,9 @@ class Case:
                 kernels=("k_wgrad_tc (tcgen05), k_wgrad_reduce"
                          if self.dtype in ("f16", "bf16") and cin % 64 == 0 and cout % 64 == 0
                          else "k_wgrad_partial, k_wgrad_reduce"), launches=2))
+
+    def perm_or_none(self):
+        return self.perm if getattr(self, "grouped", False) else None
 
     def fwd_kernel(self, dgrad=False):
         """Kernels one forward (or dinput) call launches, following the library's
@@ -599,7 +626,9 @@ def record_traffic(csv_path: str, workload: str, phases):
         got["outcoords"] = per_call(k(r"k_(candidates|radix|scan|unique|bm_)"),
                                     r"k_(candidates|bm_mark)")
     if "build" in phases:
-        got["build"] = per_call(k(r"k_(build_init|hash_insert|map_probe)"), r"k_map_probe")
+        # a submanifold build with its row order also runs the mask-key sort
+        ro = r"|row_keys_from_mask|radix|scan_exclusive|perm_from_keys" if k(r"k_row_keys_from_mask") else ""
+        got["build"] = per_call(k(r"k_(build_init|hash_insert|map_probe" + ro + ")"), r"k_map_probe")
     conv = k(r"k_(conv_|gather_gemm)")
     fwd, dgr = (conv[0::2], conv[1::2]) if "dgrad" in phases else (conv, [])
     tr = k(r"k_(transpose_w|i8_split_w)")
@@ -795,7 +824,7 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
     if case_w.get("int8"):
         # the oracle's int8 rule on a sample of output rows (the map charged pro rata)
         per_row = 2.0 * float(cnt.sum()) / max(n, 1) * cin * cout
-        rows = int(min(n, max(64, budget_s * 0.5e9 / max(per_row, 1.0))))
+        rows = int(min(n, max(64, budget_s * 0.5e9 * _THREADS[0] / max(per_row, 1.0))))
         sel = np.linspace(0, n - 1, rows).astype(np.int64)
         t1 = time.perf_counter()
         oracle.conv_fwd_int8(case_w["x"], case_w["w"], case_w["scale"], case_w["bias"],
@@ -812,7 +841,7 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
         _, imap_t, cnt = oracle.strided_map(c, oc, batch, shape, ks, stride, pad, 1, True)
         y64 = oracle.f64(case_w["y_for"](oc.shape[0]))
         per_row = 2.0 * float(cnt.sum()) / max(n, 1) * cin * cout
-        rows = int(min(n, max(64, budget_s * 1.0e9 / max(per_row, 1.0))))
+        rows = int(min(n, max(64, budget_s * 1.0e9 * _THREADS[0] / max(per_row, 1.0))))
         sel = np.linspace(0, n - 1, rows).astype(np.int64)
         t1 = time.perf_counter()
         oracle.conv_fwd(y64, w64, b64, imap_t, rows=sel)
@@ -824,7 +853,7 @@ def cpu_sample(case_w, batch, shape, ks, subm, pairs_total, budget_s, stride=1, 
     n_out = imap.shape[1]
     per_row = 2.0 * float(cnt.sum()) / max(n_out, 1) * cin * cout  # flops per output row
     # rows so that the forward sample takes about the budget at ~1 GFLOP/s
-    rows = int(min(n_out, max(64, budget_s * 1.0e9 / max(per_row, 1.0))))
+    rows = int(min(n_out, max(64, budget_s * 1.0e9 * _THREADS[0] / max(per_row, 1.0))))
     sel = np.linspace(0, n_out - 1, rows).astype(np.int64) if rows < n_out else None
     reps, flops, t_fwd = 0, 0.0, 0.0
     t1 = time.perf_counter()
@@ -906,9 +935,13 @@ def main():
     ap.add_argument("--workload", choices=sorted(DESCRIPTIONS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--row-order", choices=["on", "off"], default="off",
+                    help="compute the wide-channel submanifold convs' tiles in mask-grouped "
+                         "row order (built with the map) or in map order")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="store the DRAM bytes of an ncu metrics log of this workload and exit")
     args = ap.parse_args()
+    ROW_ORDER[0] = args.row_order == "on"
     if args.record_traffic:
         w = scenes.workload(args.workload)
         phases = (["build"] if w["subm"] and w["k"] > 1 else []) + \

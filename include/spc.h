@@ -270,19 +270,28 @@ SPC_API spc_status spc_conv_fwd(const void* x, const void* w, const void* bias,
  * accumulators, before the single rounding to dt, so the output is written in
  * one pass and the residual read once.
  *
+ *  perm       [n_out] int32 or NULL: a row order from spc_map_row_order(imap)
+ *             (rows grouped by offset mask; pass its mask as `mask`).  The
+ *             tensor-core kernel then computes its row tiles in that order and
+ *             a tile runs only the offsets its rows use: on submanifold shells
+ *             that cuts the tiles' zero-filled rows from about a fifth of the
+ *             gathered slots to a few percent (spconv's mask-sorted implicit
+ *             GEMM, the `do_sort` of "Optimize Int8 Kernels by Disabling Sort
+ *             in Implicit Gemm").  The result is the same; K <= 32.
  *  residual   [n_out, cout] of dtype dt, 16-byte aligned, or NULL (no add);
  *             it must not be y itself.
  *  add_scale  factor of the residual (1.0 for a plain residual add).
  *  act        SPC_ACT_NONE or SPC_ACT_RELU.
  *  All other arguments, the kernels and the errors as for spc_conv_fwd, which is
- *  this call with residual NULL and SPC_ACT_NONE.
+ *  this call with perm and residual NULL and SPC_ACT_NONE.
  */
 SPC_API spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias,
-                                      const int32_t* imap, const uint32_t* mask, int32_t K,
-                                      int64_t n_in, int64_t n_out, int32_t cin, int32_t cout,
-                                      spc_dtype dt, spc_precision prec, const void* residual,
-                                      float add_scale, spc_activation act, void* y,
-                                      int32_t* status, void* ws, size_t ws_bytes, void* stream);
+                                      const int32_t* imap, const uint32_t* mask,
+                                      const int32_t* perm, int32_t K, int64_t n_in, int64_t n_out,
+                                      int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec,
+                                      const void* residual, float add_scale, spc_activation act,
+                                      void* y, int32_t* status, void* ws, size_t ws_bytes,
+                                      void* stream);
 
 /* spc_conv_inverse -- out[i, :] = bias + sum over pairs imap[k, o] = i of y[o, :] W[k]
  * (spconv SparseInverseConv3d, "spconv.pytorch Layer APIs Reference" and "Using
@@ -367,7 +376,9 @@ SPC_API spc_status spc_conv_fwd_int8(const int8_t* x, const int8_t* w, const flo
  * counterpart on the pages: it is how this library feeds spc_conv_inverse).
  * Computed once per map, like the map itself.
  *
- *  map   [K, n] int32, K <= 32.   mask [n] uint32 out or NULL.
+ *  map   [K, n] int32, K <= 32, and mask [n] uint32 out (or NULL); or map NULL
+ *        and mask [n] in: the row masks spc_build_indice_map already wrote for
+ *        that map (the K x n map is then not read).
  *  perm  [n] int32 out: a permutation of 0 .. n-1.
  *  ws    spc_map_row_order_workspace_size(n) bytes.
  */
@@ -418,19 +429,23 @@ SPC_API spc_status spc_maxpool_dgrad(const void* dy, const int32_t* imap_t, cons
  *  map   see spc_map_kind: imap_t [K, n_in] (SPC_MAP_TRANSPOSED) or the
  *        submanifold imap [K, n] (SPC_MAP_SUBM_MIRROR, n_in == n_out); NULL
  *        when K == 1 and n_in == n_out (dx = dy W[0]^T).
- *  mask  NULL, or with SPC_MAP_SUBM_MIRROR (K <= 32) the row mask that
- *        spc_build_indice_map wrote for that submanifold map (the kernel
- *        mirrors its bits itself).
+ *  mask  NULL, or (K <= 32) with SPC_MAP_SUBM_MIRROR the row mask that
+ *        spc_build_indice_map (or spc_map_row_order) wrote for that submanifold
+ *        map (the kernel mirrors its bits itself), with SPC_MAP_TRANSPOSED the
+ *        mask spc_map_row_order wrote for imap_t.
+ *  perm  [n_in] int32 or NULL: a row order of the input rows (for a
+ *        submanifold map, the forward's spc_map_row_order(imap) order serves:
+ *        mirrored masks group the same way), as for spc_conv_fwd_fused.
  *  dx    [n_in, cin] of dtype dt out.
  *  status  device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
  *  Kernels as for spc_conv_fwd with the roles of Cin and Cout exchanged; no
  *  workspace is needed.
  */
 SPC_API spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map,
-                                  spc_map_kind kind, const uint32_t* mask, int32_t K, int64_t n_in,
-                                  int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
-                                  spc_precision prec, void* dx, int32_t* status, void* ws,
-                                  size_t ws_bytes, void* stream);
+                                  spc_map_kind kind, const uint32_t* mask, const int32_t* perm,
+                                  int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
+                                  int32_t cout, spc_dtype dt, spc_precision prec, void* dx,
+                                  int32_t* status, void* ws, size_t ws_bytes, void* stream);
 
 /* spc_conv_wgrad -- dW[k] = sum_{o: imap[k, o] = i != -1} x[i, :]^T dy[o, :],
  * reduced in fp32 over all active pairs ("dfilter" in the HYGON-AI spconv-das

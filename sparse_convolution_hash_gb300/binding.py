@@ -111,7 +111,7 @@ def lib():
             L.spc_conv_fwd.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
                                        _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd.restype = _i32
-            L.spc_conv_fwd_fused.argtypes = [_p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
+            L.spc_conv_fwd_fused.argtypes = [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32, _i32,
                                              _i32, _p, ctypes.c_float, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd_fused.restype = _i32
             L.spc_maxpool_fwd.argtypes = [_p, _p, _p, _i32, _i64, _i64, _i32, _i32, _p, _p, _p]
@@ -130,7 +130,7 @@ def lib():
             L.spc_conv_fwd_int8.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i32, _i32,
                                             _p, ctypes.c_float, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_fwd_int8.restype = _i32
-            L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _i32, _i64, _i64, _i32, _i32,
+            L.spc_conv_dgrad.argtypes = [_p, _p, _p, _i32, _p, _p, _i32, _i64, _i64, _i32, _i32,
                                          _i32, _i32, _p, _p, _p, _sz, _p]
             L.spc_conv_dgrad.restype = _i32
             L.spc_conv_wgrad_workspace_size.argtypes = [_i32, _i64, _i64, _i32, _i32, _i32]
@@ -283,11 +283,16 @@ def spc_conv_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
                  imap: Optional[torch.Tensor], mask: Optional[torch.Tensor] = None,
                  n_out: Optional[int] = None, precision: int = SPC_PREC_EXACT,
                  out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                 ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+                 ws: Optional[torch.Tensor] = None, perm: Optional[torch.Tensor] = None) -> torch.Tensor:
     """y[o] = bias + sum over pairs of x[imap[k, o]] W[k]; y has x's dtype.
 
     Pass `out`, `ws` (spc_conv_workspace_size bytes) and `status` to call
-    without allocating (e.g. inside CUDA-graph capture)."""
+    without allocating (e.g. inside CUDA-graph capture).  `perm` (with its
+    `mask`) from spc_map_row_order(imap) computes the tiles in that row order
+    (through spc_conv_fwd_fused, which takes it)."""
+    if perm is not None:
+        return spc_conv_fwd_fused(x, w, bias, imap, mask, n_out=n_out, precision=precision,
+                                  out=out, status=status, ws=ws, perm=perm)
     x = _cuda(x, "x")
     w = _cuda(w, "w").to(x.dtype)
     b = _cuda(bias, "bias").to(x.dtype) if bias is not None else None
@@ -318,8 +323,10 @@ def spc_conv_fwd_fused(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Te
                        act: int = SPC_ACT_NONE, n_out: Optional[int] = None,
                        precision: int = SPC_PREC_EXACT, out: Optional[torch.Tensor] = None,
                        status: Optional[torch.Tensor] = None,
-                       ws: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """y[o] = act(bias + sum over pairs of x[imap[k, o]] W[k] + add_scale residual[o])."""
+                       ws: Optional[torch.Tensor] = None,
+                       perm: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y[o] = act(bias + sum over pairs of x[imap[k, o]] W[k] + add_scale residual[o]);
+    `perm` (with its `mask`) from spc_map_row_order(imap) groups the tiles' rows."""
     x = _cuda(x, "x")
     w = _cuda(w, "w").to(x.dtype)
     b = _cuda(bias, "bias").to(x.dtype) if bias is not None else None
@@ -335,7 +342,7 @@ def spc_conv_fwd_fused(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Te
     nbytes = int(lib().spc_conv_workspace_size(K, x.shape[0], n_out, cin, cout, dt))
     if nbytes and (ws is None or ws.numel() < nbytes):
         ws = _workspace(nbytes, x.device)
-    code = lib().spc_conv_fwd_fused(_ptr(x), _ptr(w), _ptr(b), _ptr(imap), _ptr(mask), K,
+    code = lib().spc_conv_fwd_fused(_ptr(x), _ptr(w), _ptr(b), _ptr(imap), _ptr(mask), _ptr(perm), K,
                                     x.shape[0], n_out, cin, cout, dt, precision, _ptr(res),
                                     float(add_scale), int(act), _ptr(y), _ptr(status), _ptr(ws),
                                     0 if ws is None else ws.numel(), _stream(x.device))
@@ -376,17 +383,29 @@ def spc_maxpool_dgrad(dy: torch.Tensor, imap_t: torch.Tensor, arg: torch.Tensor,
     return dx
 
 
-def spc_map_row_order(map_: torch.Tensor, ws: Optional[torch.Tensor] = None):
-    """(mask [n] uint32, perm [n] int32): rows of map [K, n] grouped by offset mask."""
-    m = _cuda(map_, "map")
-    K, n = m.shape
-    mask = torch.empty(n, dtype=torch.int32, device=m.device)
-    perm = torch.empty(n, dtype=torch.int32, device=m.device)
+def spc_map_row_order(map_: Optional[torch.Tensor], ws: Optional[torch.Tensor] = None,
+                      mask: Optional[torch.Tensor] = None, K: Optional[int] = None,
+                      perm: Optional[torch.Tensor] = None):
+    """(mask [n] uint32, perm [n] int32): rows of map [K, n] grouped by offset mask.
+
+    With map_ None, `mask` (the row masks spc_build_indice_map wrote) and `K`
+    are read instead of the map.  Passing `ws` and `perm` (and `mask`) avoids
+    allocation (e.g. inside CUDA-graph capture)."""
+    if map_ is not None:
+        m = _cuda(map_, "map")
+        K, n = m.shape
+        dev = m.device
+        mask = torch.empty(n, dtype=torch.int32, device=dev) if mask is None else mask
+    else:
+        m = None
+        assert mask is not None and K is not None
+        n, dev = mask.shape[0], mask.device
+    perm = torch.empty(n, dtype=torch.int32, device=dev) if perm is None else perm
     nbytes = int(lib().spc_map_row_order_workspace_size(n))
     if ws is None or ws.numel() < nbytes:
-        ws = _workspace(nbytes, m.device)
-    code = lib().spc_map_row_order(_ptr(m), K, n, _ptr(mask), _ptr(perm), _ptr(ws), ws.numel(),
-                                   _stream(m.device))
+        ws = _workspace(nbytes, dev)
+    code = lib().spc_map_row_order(_ptr(m), int(K), n, _ptr(mask), _ptr(perm), _ptr(ws), ws.numel(),
+                                   _stream(dev))
     _check(code, "spc_map_row_order")
     return mask, perm
 
@@ -455,15 +474,17 @@ def spc_conv_fwd_int8(x: torch.Tensor, w: torch.Tensor, scale: torch.Tensor,
 def spc_conv_dgrad(dy: torch.Tensor, w: torch.Tensor, map_: Optional[torch.Tensor], kind: int,
                    n_in: int, precision: int = SPC_PREC_EXACT, mask: Optional[torch.Tensor] = None,
                    out: Optional[torch.Tensor] = None,
-                   status: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """dx[i] = sum over pairs imap[k, o] = i of W[k] dy[o]."""
+                   status: Optional[torch.Tensor] = None,
+                   perm: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dx[i] = sum over pairs imap[k, o] = i of W[k] dy[o]; `perm` orders the
+    input-row tiles (for a submanifold map, the forward's row order)."""
     dy = _cuda(dy, "dy")
     w = _cuda(w, "w").to(dy.dtype)
     K, cin, cout = w.shape
     m = _cuda(map_, "map") if map_ is not None else None
     dx = torch.empty((n_in, cin), dtype=dy.dtype, device=dy.device) if out is None else out
     dt = _DTYPES[dy.dtype]
-    code = lib().spc_conv_dgrad(_ptr(dy), _ptr(w), _ptr(m), kind, _ptr(mask), K, n_in,
+    code = lib().spc_conv_dgrad(_ptr(dy), _ptr(w), _ptr(m), kind, _ptr(mask), _ptr(perm), K, n_in,
                                 dy.shape[0], cin, cout, dt, precision, _ptr(dx), _ptr(status),
                                 None, 0, _stream(dy.device))
     _check(code, "spc_conv_dgrad")

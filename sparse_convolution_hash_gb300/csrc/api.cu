@@ -333,12 +333,14 @@ spc_status conv_fwd_impl(const void* x, const void* w, const void* bias, const i
 }  // namespace
 
 spc_status spc_conv_fwd_fused(const void* x, const void* w, const void* bias, const int32_t* imap,
-                              const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
-                              int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec,
-                              const void* residual, float add_scale, spc_activation act, void* y,
-                              int32_t* status, void* ws, size_t ws_bytes, void* stream)
+                              const uint32_t* mask, const int32_t* perm, int32_t K, int64_t n_in,
+                              int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
+                              spc_precision prec, const void* residual, float add_scale,
+                              spc_activation act, void* y, int32_t* status, void* ws,
+                              size_t ws_bytes, void* stream)
 {
-    return conv_fwd_impl(x, w, bias, imap, mask, nullptr, K, n_in, n_out, cin, cout, dt, prec,
+    if (perm && K > 32) return SPC_ERR_INVALID_ARG;
+    return conv_fwd_impl(x, w, bias, imap, mask, perm, K, n_in, n_out, cin, cout, dt, prec,
                          residual, add_scale, act, y, status, ws, ws_bytes, stream);
 }
 
@@ -404,7 +406,7 @@ spc_status spc_map_row_order(const int32_t* map, int32_t K, int64_t n, uint32_t*
                              int32_t* perm, void* ws, size_t ws_bytes, void* stream)
 {
     if (K < 1 || K > 32 || n < 0) return SPC_ERR_INVALID_ARG;
-    if (n > 0 && (!map || !perm)) return SPC_ERR_INVALID_ARG;
+    if (n > 0 && ((!map && !mask) || !perm)) return SPC_ERR_INVALID_ARG;
     if (n > INT32_MAX - 1) return SPC_ERR_UNSUPPORTED;
     return map_row_order(map, K, n, mask, perm, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
@@ -445,9 +447,10 @@ spc_status spc_conv_inverse(const void* y, const void* w, const void* bias, cons
 }
 
 spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc_map_kind kind,
-                          const uint32_t* mask, int32_t K, int64_t n_in, int64_t n_out,
-                          int32_t cin, int32_t cout, spc_dtype dt, spc_precision prec, void* dx,
-                          int32_t* status, void* ws, size_t ws_bytes, void* stream)
+                          const uint32_t* mask, const int32_t* perm, int32_t K, int64_t n_in,
+                          int64_t n_out, int32_t cin, int32_t cout, spc_dtype dt,
+                          spc_precision prec, void* dx, int32_t* status, void* ws,
+                          size_t ws_bytes, void* stream)
 {
     (void)ws;
     (void)ws_bytes;
@@ -457,7 +460,7 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
     if (kind != SPC_MAP_TRANSPOSED && kind != SPC_MAP_SUBM_MIRROR) return SPC_ERR_INVALID_ARG;
     if (kind == SPC_MAP_SUBM_MIRROR && n_in != n_out) return SPC_ERR_INVALID_ARG;
     if (!map && n_in > 0 && !(K == 1 && n_in == n_out)) return SPC_ERR_INVALID_ARG;
-    if (mask && (K > 32 || kind != SPC_MAP_SUBM_MIRROR)) return SPC_ERR_INVALID_ARG;
+    if ((mask || perm) && K > 32) return SPC_ERR_INVALID_ARG;
     GatherGemm p;
     p.in = dy;
     p.w = w;
@@ -493,7 +496,7 @@ spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* map, spc
         a.cred = cout;
         a.n_total = cin;
         a.mirror = p.mirror;
-        a.perm = nullptr;
+        a.perm = perm;
         a.residual = nullptr;
         a.add_scale = 0.f;
         a.act = 0;

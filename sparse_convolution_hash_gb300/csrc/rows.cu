@@ -29,6 +29,18 @@ k_row_mask_keys(const int32_t* __restrict__ map, int K, int64_t n, uint32_t* __r
     keys[i] = ((unsigned long long)bits << 32) | (unsigned long long)i;
 }
 
+// Keys from masks a build already wrote (no map read).
+__global__ void __launch_bounds__(kBlock)
+k_row_keys_from_mask(const uint32_t* __restrict__ mask, int K, int64_t n,
+                     unsigned long long* __restrict__ keys, unsigned long long* __restrict__ counter)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i == 0) *counter = (unsigned long long)n;
+    if (i >= n) return;
+    const uint32_t bits = __ldg(mask + i) & (K >= 32 ? 0xffffffffu : ((1u << K) - 1u));
+    keys[i] = ((unsigned long long)bits << 32) | (unsigned long long)i;
+}
+
 __global__ void __launch_bounds__(kBlock)
 k_perm_from_keys(const unsigned long long* __restrict__ keys, int64_t n, int32_t* __restrict__ perm)
 {
@@ -76,7 +88,10 @@ spc_status map_row_order(const int32_t* map, int32_t K, int64_t n, uint32_t* mas
     RowWs w;
     carve(n, static_cast<char*>(ws), &w);
     const unsigned grid = (unsigned)ceil_div(n, (int64_t)kBlock);
-    k_row_mask_keys<<<grid, kBlock, 0, st>>>(map, K, n, mask, w.keys_a, w.counter);
+    if (map)
+        k_row_mask_keys<<<grid, kBlock, 0, st>>>(map, K, n, mask, w.keys_a, w.counter);
+    else
+        k_row_keys_from_mask<<<grid, kBlock, 0, st>>>(mask, K, n, w.keys_a, w.counter);
     SPC_LAUNCH_CHECK();
     const spc_status s = radix_sort_keys(w.keys_a, w.keys_b, w.counter, n, 32, 32 + K, w.radix, st);
     if (s != SPC_OK) return s;

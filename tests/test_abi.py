@@ -115,12 +115,12 @@ def test_argument_errors_return_before_any_work(L):
                           None) == E
     # fused forward: unknown activation, misaligned residual, residual aliasing the output
     fz = L.spc_conv_fwd_fused
-    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, None, 27, 4,
               4, 8, 8, 0, 0, None, 1.0, 2, ctypes.c_void_p(512), None, None, 0, None) == E
-    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, None, 27, 4,
               4, 8, 8, 0, 0, ctypes.c_void_p(260), 1.0, 1, ctypes.c_void_p(512), None, None, 0,
               None) == E
-    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, 27, 4,
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None, None, 27, 4,
               4, 8, 8, 0, 0, ctypes.c_void_p(512), 1.0, 1, ctypes.c_void_p(512), None, None, 0,
               None) == E
     # max pool: offsets beyond the uint8 argmax, a mask with K > 32, a missing map
@@ -162,12 +162,15 @@ def test_argument_errors_return_before_any_work(L):
                           None, 27, 4, 4, 32, 128, binding.SPC_BF16, 0, ctypes.c_void_p(256),
                           None, None, 0, None) == 8
     assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
-                            binding.SPC_MAP_SUBM_MIRROR, None, 27, 4, 5, 8, 8, 0, 0,
+                            binding.SPC_MAP_SUBM_MIRROR, None, None, 27, 4, 5, 8, 8, 0, 0,
                             ctypes.c_void_p(256), None, None, 0, None) == E
-    # a mask is only accepted with a submanifold map
+    # a mask or a row order needs K <= 32
     assert L.spc_conv_dgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256),
-                            binding.SPC_MAP_TRANSPOSED, ctypes.c_void_p(256), 27, 4, 4, 8, 8, 0, 0,
-                            ctypes.c_void_p(256), None, None, 0, None) == E
+                            binding.SPC_MAP_TRANSPOSED, None, ctypes.c_void_p(256), 125, 4, 4, 8, 8,
+                            0, 0, ctypes.c_void_p(256), None, None, 0, None) == E
+    assert fz(ctypes.c_void_p(256), ctypes.c_void_p(256), None, ctypes.c_void_p(256), None,
+              ctypes.c_void_p(256), 125, 4, 4, 8, 8, 0, 0, None, 1.0, 0, ctypes.c_void_p(512),
+              None, None, 0, None) == E
     assert L.spc_conv_wgrad(ctypes.c_void_p(256), ctypes.c_void_p(256), ctypes.c_void_p(256), 27,
                             4, 4, 8, 8, 2, 0, ctypes.c_void_p(256), None, None, 0, None) == 8
     # strided out coords: null n_out / status

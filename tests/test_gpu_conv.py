@@ -428,3 +428,29 @@ def test_k1_dense_rows(dtype, n, cin, cout):
     assert normwise(to_np(y), oracle.conv_fwd(x, w, b, ident)) < TOL[(dtype, "exact")]
     dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), None, spc.SPC_MAP_SUBM_MIRROR, n)
     assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, ident, n)) < TOL[(dtype, "exact")]
+
+
+@pytest.mark.parametrize("n,cin,cout", [(2100, 64, 128), (3000, 64, 64), (1000, 128, 128),
+                                        (700, 192, 64), (600, 16, 64)])
+def test_row_order_forward_and_dinput(n, cin, cout):
+    """Tiles in mask-grouped row order (spc_map_row_order, from the map or from
+    the build's masks): forward and dinput against the oracle and equal to the
+    map-order results."""
+    g = np.random.default_rng(n + 7)
+    batch, shape = 2, (12, 11, 13)
+    coords = rand_coords(g, n, batch, shape)
+    x, w, b, dy, m, imap_ref = subm_case(coords, batch, shape, cin, cout, "bf16", seed=n)
+    d = dev()
+    mask_g, perm = spc.spc_map_row_order(m["imap"])
+    mask_b, perm_b = spc.spc_map_row_order(None, mask=m["mask"].clone(), K=27)
+    assert torch.equal(perm, perm_b) and torch.equal(mask_g, mask_b)
+    assert torch.equal(torch.sort(perm.long()).values, torch.arange(n, device=d))
+    y0 = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], m["mask"])
+    y = spc.spc_conv_fwd(x.to(d), w.to(d), b.to(d), m["imap"], mask_g, perm=perm)
+    assert normwise(to_np(y), oracle.conv_fwd(x, w, b, imap_ref)) < 2e-2
+    assert torch.equal(y, y0)
+    dx0 = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, mask=m["mask"])
+    dx = spc.spc_conv_dgrad(dy.to(d), w.to(d), m["imap"], spc.SPC_MAP_SUBM_MIRROR, n, mask=mask_g,
+                            perm=perm)
+    assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, n)) < 2e-2
+    assert torch.equal(dx, dx0)
