@@ -365,7 +365,7 @@ class Case:
                                                         mask_t=self.mask_t, perm=self.perm),
                 "conv", s * n_out * cin + s * n * cout + s * K * cin * cout + 4 * P,
                 2.0 * P * cin * cout, kernels=self.fwd_kernel(),
-                launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+                launches=2 if "k_transpose_w" in self.fwd_kernel() else 1))
             return
         self.inverse = False
         self.y = torch.empty((n_out, cout), dtype=self.x.dtype, device=dev)
@@ -382,7 +382,7 @@ class Case:
                     out=self.y, status=self.status, ws=self.conv_ws, perm=self.perm_or_none()),
                 "conv", s * n * cin + 2 * s * n_out * cout + s * K * cin * cout + 4 * P + bias_b,
                 flops, kernels=self.fwd_kernel() + ", fused residual + ReLU epilogue",
-                launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+                launches=2 if "k_transpose_w" in self.fwd_kernel() else 1))
         else:
             self.phases.append(Phase(
                 "fwd", lambda: spc.spc_conv_fwd(self.x, self.wt, self.bias, self.imap, self.mask,
@@ -390,7 +390,7 @@ class Case:
                                                 status=self.status, ws=self.conv_ws,
                                                 perm=self.perm_or_none()),
                 "conv", s * n * cin + s * n_out * cout + s * K * cin * cout + 4 * P + bias_b, flops,
-                kernels=self.fwd_kernel(), launches=2 if "tcgen05" in self.fwd_kernel() else 1))
+                kernels=self.fwd_kernel(), launches=2 if "k_transpose_w" in self.fwd_kernel() else 1))
         self.train = bool(w.get("train"))
         if self.train:
             self.dy = w["dy"].to(dev)
@@ -431,7 +431,10 @@ class Case:
             (half and cred in (16, 32) and (co in (16, 32) or co % 64 == 0)) or
             (self.dtype == "f32" and self.prec == self.B.SPC_PREC_TF32 and cred % 32 == 0 and co % 64 == 0))
         if tc:
-            return "k_conv_tc (tcgen05)" + ("" if dgrad else " + k_transpose_w")
+            as_stored = half and cred % 64 == 0 and co % 64 == 0  # W read as stored
+            dense = self.K == 1 and half and cred % 64 == 0 and co % 64 == 0
+            return ("k_conv_tc (tcgen05" + (", dense TMA rows" if dense else "") + ")" +
+                    ("" if dgrad or as_stored else " + k_transpose_w"))
         return "k_gather_gemm_simt"
 
     def conv_flops(self):
