@@ -5,19 +5,27 @@
 // with Calculated Scales and Bias").
 //
 // sm_103a has no integer MMA (ptxas rejects tcgen05.mma .kind::i8 for this
-// target), so the integer sums are formed exactly on the fp16 path:
-//   * every int8 feature value is exact in fp16 (|v| <= 128 < 2^11);
-//   * each weight is split as w = 16 * hi + lo with hi in [-8, 7] and lo in
-//     [0, 15] (both exact in fp16), prepared once per call in the workspace as
-//     a K-major B operand of 2 * BN rows per CTA: the hi rows, then the lo rows;
-//   * one MMA of N = 2 * BN accumulates sum x * hi and sum x * lo side by side
-//     in fp32 tensor memory.  Every product and every partial sum is an integer
-//     of magnitude below 2^24 as long as K * Cin <= 8192 (|x * lo| <= 1920), so
-//     fp32 holds them exactly, whatever the summation order;
-//   * the epilogue forms acc = 16 * hi_sum + lo_sum in int32 (exact), then
-//     f = float(acc) * scale + bias (+ add_scale * float(add)), ReLU, rounds half
-//     away from zero and saturates to [-128, 127], each fp32 operation rounded
-//     once in that order.
+// target), so the integer sums are formed exactly on the fp16 path.  Every
+// int8 value is exact in fp16 (|v| <= 128 < 2^11), every product of two is an
+// exact fp32 integer (|x w| <= 2^14), and a sum of integers stays exact in fp32
+// while every partial sum is below 2^24 in magnitude, whatever the order.  Two
+// ways keep the partial sums in range:
+//   * several accumulators (NACC > 0): stage t (64 input channels of one
+//     offset) accumulates into tensor-memory accumulator t % NACC, so an
+//     accumulator sums at most 15 stages (960 products, |sum| < 2^24), and the
+//     epilogue adds the NACC accumulators in int32.  The weights are only
+//     widened to fp16 (a K-major B operand of BN rows per CTA); the MMA is
+//     N = BN wide.  Needs K * Cin / 64 <= 15 NACC with NACC * BN <= 512 TMEM
+//     columns (K * Cin <= 7680);
+//   * a 4-bit weight split (NACC = 0, up to K * Cin = 8192): w = 16 * hi + lo,
+//     hi in [-8, 7], lo in [0, 15], prepared once per call as a K-major B
+//     operand of 2 * BN rows per CTA (the hi rows, then the lo rows); one MMA
+//     of N = 2 * BN accumulates sum x * hi and sum x * lo side by side
+//     (|x * lo| <= 1920, so 8192 products stay below 2^24), and the epilogue
+//     forms acc = 16 * hi_sum + lo_sum in int32.
+// The epilogue then computes f = float(acc) * scale + bias (+ add_scale *
+// float(add)), ReLU, rounds half away from zero and saturates to [-128, 127],
+// each fp32 operation rounded once in that order.
 //
 // The gather stays on int8 rows (half the bytes of a 16-bit row): gather warps
 // copy each tile row's 64-byte int8 chunk with 16-byte cp.async into a raw
@@ -41,19 +49,22 @@ constexpr int kRows = 128;  // output rows per CTA (one MMA of M = 128)
 constexpr int kCh = 64;     // input channels per stage (128 bytes of fp16)
 constexpr uint64_t kDrainNs = 2000000000ull;  // bound of the waits for a CTA's own copies / MMAs
 
-template <int BN, int STAGES, int NW, int RAW>
+template <int BN, int STAGES, int NW, int RAW, int NACC>
 struct I8Shape {
     static constexpr int kWorkers = NW * 32;
     static constexpr int kThreads = kWorkers + 64;
     static constexpr int kTmaWarp = NW, kMmaWarp = NW + 1;
     static constexpr int A_BYTES = kRows * 128;         // 128 rows x 64 fp16
-    static constexpr int B_BYTES = 2 * BN * 128;        // hi and lo rows x 64 fp16
+    static constexpr int BROWS = NACC ? BN : 2 * BN;    // B rows: the weights, or their hi and lo halves
+    static constexpr int B_BYTES = BROWS * 128;         // x 64 fp16
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int RAW_BYTES = kRows * kCh;       // 128 rows x 64 int8
     static constexpr int PIECES = kRows * kCh / 16;     // 16-byte pieces per stage
     static constexpr int PER_THREAD = PIECES / kWorkers;
-    static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : 256;
-    static constexpr int kMinCtas = BN == 64 ? 2 : 1;
+    static constexpr int ACC_COLS = NACC ? NACC * BN : 2 * BN;
+    static constexpr int TMEM_COLS = ACC_COLS <= 128 ? 128 : (ACC_COLS <= 256 ? 256 : 512);
+    static constexpr int kMinCtas = TMEM_COLS <= 128 && STAGES <= 2 ? 2 : 1;
+    static_assert(ACC_COLS <= 512, "tensor memory");
     static_assert(PIECES % kWorkers == 0, "pieces per thread");
     static size_t smem_bytes(int K)
     {
@@ -79,11 +90,11 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-template <int BN, int STAGES, int NW, int RAW>
-__global__ void __launch_bounds__(I8Shape<BN, STAGES, NW, RAW>::kThreads, I8Shape<BN, STAGES, NW, RAW>::kMinCtas)
+template <int BN, int STAGES, int NW, int RAW, int NACC>
+__global__ void __launch_bounds__(I8Shape<BN, STAGES, NW, RAW, NACC>::kThreads, I8Shape<BN, STAGES, NW, RAW, NACC>::kMinCtas)
 k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
 {
-    using S = I8Shape<BN, STAGES, NW, RAW>;
+    using S = I8Shape<BN, STAGES, NW, RAW, NACC>;
     constexpr int kWorkers = S::kWorkers, kTmaWarp = S::kTmaWarp, kMmaWarp = S::kMmaWarp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -185,7 +196,7 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
         }
         ptx::cp_async_wait_all();  // nothing of ours may still land when the CTA ends
     } else if (warp == kTmaWarp) {
-        // ------------------------------------------ split weights (TMA, K-major)
+        // ---------------------------------- fp16 weights or halves (TMA, K-major)
         int issued = 0;
         if (lane == 0) {
             const int nblk = a.cout / BN;
@@ -199,7 +210,7 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
                 const int c0 = (it % kchunks) * kCh;
                 const uint32_t b_dst = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES + S::A_BYTES);
                 ptx::mbar_arrive_expect_tx(&full[s], S::B_BYTES);
-                ptx::tma_tile2d(b_dst, &tma_b, c0, (k * nblk + blk) * 2 * BN, &full[s]);
+                ptx::tma_tile2d(b_dst, &tma_b, c0, (k * nblk + blk) * S::BROWS, &full[s]);
                 ++issued;
             }
             const int first = issued > STAGES ? issued - STAGES : 0;
@@ -208,7 +219,7 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
         }
     } else if (warp == kMmaWarp && lane == 0) {
         // ------------------------------------------------------- MMA issuer
-        const uint32_t idesc = ptx::idesc_make(0 /* fp16 */, kRows, 2 * BN);
+        const uint32_t idesc = ptx::idesc_make(0 /* fp16 */, kRows, S::BROWS);
         for (int it = 0; it < n_iter; ++it) {
             const int s = it % STAGES;
             if (!ptx::mbar_wait(&full[s], (it / STAGES) & 1, a.wait_ns)) {
@@ -219,9 +230,13 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
             const uint32_t a_base = ptx::smem_u32(smem + (size_t)s * S::STAGE_BYTES);
             const uint64_t ad = ptx::desc_k_sw<128>(a_base);
             const uint64_t bd = ptx::desc_k_sw<128>(a_base + S::A_BYTES);
+            // several accumulators: stage it goes to accumulator it % NACC, whose
+            // first stage overwrites it
+            const uint32_t d = NACC ? tmem + (uint32_t)((it % (NACC ? NACC : 1)) * BN) : tmem;
+            const bool first = NACC ? it < NACC : it == 0;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // 16 channels (32 bytes) of K per instruction
-                ptx::mma<0>(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (it | kk) != 0 ? 1u : 0u);
+                ptx::mma<0>(d, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
             ptx::mma_commit(&empty[s]);
         }
         ptx::mma_commit(done);
@@ -243,15 +258,34 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
         } else {
 #pragma unroll 1
             for (int c = cgrp * kGroupCols; c < (cgrp + 1) * kGroupCols; c += 16) {
-                uint32_t vh[16], vl[16];
-                if (n_iter > 0) {
-                    const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16);
-                    ptx::tmem_ld16(ta + (uint32_t)c, vh);
-                    ptx::tmem_ld16(ta + (uint32_t)(BN + c), vl);
-                    ptx::tmem_ld_wait();
-                } else {
+                int acc[16];
+                if (NACC) {
+                    // the sum of the accumulators that received stages (exact integers)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) vh[j] = vl[j] = 0u;
+                    for (int j = 0; j < 16; ++j) acc[j] = 0;
+                    const int na = n_iter < NACC ? n_iter : NACC;
+                    for (int q = 0; q < na; ++q) {
+                        uint32_t v[16];
+                        ptx::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(q * BN + c), v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] += __float2int_rn(__uint_as_float(v[j]));
+                    }
+                } else {
+                    uint32_t vh[16], vl[16];
+                    if (n_iter > 0) {
+                        const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16);
+                        ptx::tmem_ld16(ta + (uint32_t)c, vh);
+                        ptx::tmem_ld16(ta + (uint32_t)(BN + c), vl);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) vh[j] = vl[j] = 0u;
+                    }
+                    // exact integers: |hi sum| < 2^23, 0 <= |lo sum| < 2^24
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        acc[j] = __float2int_rn(__uint_as_float(vh[j])) * 16 + __float2int_rn(__uint_as_float(vl[j]));
                 }
                 const int n = n0 + c;
                 alignas(16) int8_t add[16];
@@ -262,10 +296,7 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
                 alignas(16) int8_t o[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    // exact integers: |hi sum| < 2^23, 0 <= |lo sum| < 2^24
-                    const int acc = __float2int_rn(__uint_as_float(vh[j])) * 16 +
-                                    __float2int_rn(__uint_as_float(vl[j]));
-                    float f = __fmul_rn(__int2float_rn(acc), __ldg(a.scale + n + j));
+                    float f = __fmul_rn(__int2float_rn(acc[j]), __ldg(a.scale + n + j));
                     if (a.bias) f = __fadd_rn(f, __ldg(a.bias + n + j));
                     if (use_add) f = __fadd_rn(f, __fmul_rn(a.add_scale, (float)add[j]));
                     if (a.act && f < 0.f) f = 0.f;
@@ -284,40 +315,46 @@ k_conv_i8(I8Args a, const __grid_constant__ CUtensorMap tma_b)
     }
 }
 
-// wq[k][blk][r][c] (fp16, [K][cout / BN][2 BN][cin]): for r < BN the high part
-// of w[k][c][blk BN + r], else the low part of w[k][c][blk BN + r - BN], with
-// w = 16 hi + lo, hi = floor(w / 16) in [-8, 7], lo in [0, 15].
-__global__ void k_i8_split_w(const int8_t* __restrict__ w, __half* __restrict__ wq, int K, int cin,
-                             int cout, int bn)
+// wq[k][blk][r][c] (fp16, [K][cout / BN][rows][cin]).  split: rows = 2 BN, for
+// r < BN the high part of w[k][c][blk BN + r], else the low part of
+// w[k][c][blk BN + r - BN], with w = 16 hi + lo, hi = floor(w / 16) in [-8, 7],
+// lo in [0, 15].  Otherwise rows = BN and the weight itself.
+__global__ void k_i8_prep_w(const int8_t* __restrict__ w, __half* __restrict__ wq, int K, int cin,
+                            int cout, int bn, int split)
 {
-    const int64_t total = (int64_t)K * cout * 2 * cin;
+    const int rows = split ? 2 * bn : bn;
+    const int64_t total = (int64_t)K * (cout / bn) * rows * cin;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(e % cin);
         int64_t t = e / cin;
-        const int r = (int)(t % (2 * bn));
-        t /= 2 * bn;
+        const int r = (int)(t % rows);
+        t /= rows;
         const int blk = (int)(t % (cout / bn));
         const int k = (int)(t / (cout / bn));
         const int ch = blk * bn + (r < bn ? r : r - bn);
         const int v = w[((int64_t)k * cin + c) * cout + ch];
-        const int part = r < bn ? (v >> 4) : (v & 15);
+        const int part = !split ? v : (r < bn ? (v >> 4) : (v & 15));
         wq[e] = __int2half_rn(part);
     }
 }
 
 constexpr size_t kSmemPerSm = 233472, kSmemPerCta = 1024;
 
-template <int BN, int STAGES, int NW, int RAW>
-spc_status launch_i8(const I8Args& a, cudaStream_t st)
+template <int BN, int STAGES, int NW, int RAW, int NACC>
+spc_status launch_i8(const I8Args& a, const int8_t* w, cudaStream_t st)
 {
-    using S = I8Shape<BN, STAGES, NW, RAW>;
+    using S = I8Shape<BN, STAGES, NW, RAW, NACC>;
+    const int64_t total = (int64_t)a.K * (a.cout / BN) * S::BROWS * a.cin;
+    const int blocks = (int)std::min<int64_t>(ceil_div(total, 256), 4096);
+    k_i8_prep_w<<<blocks, 256, 0, st>>>(w, a.wq, a.K, a.cin, a.cout, BN, NACC ? 0 : 1);
+    SPC_LAUNCH_CHECK();
     CUtensorMap tb;
     if (!tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.wq, (uint64_t)a.cin,
-                 (uint64_t)a.K * 2 * a.cout, kCh, 2 * BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                 (uint64_t)a.K * (a.cout / BN) * S::BROWS, kCh, S::BROWS, CU_TENSOR_MAP_SWIZZLE_128B))
         return SPC_ERR_UNSUPPORTED;
     const size_t smem = S::smem_bytes(a.K);
-    auto kern = k_conv_i8<BN, STAGES, NW, RAW>;
+    auto kern = k_conv_i8<BN, STAGES, NW, RAW, NACC>;
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPC_ERR_CUDA;
@@ -341,23 +378,22 @@ bool conv_i8_supported(int32_t K, int32_t cin, int32_t cout)
     return K >= 1 && K <= 32 && cin % 64 == 0 && cout % 64 == 0 && (int64_t)K * cin <= 8192;
 }
 
-int conv_i8_bn(int32_t cout) { return cout % 128 == 0 ? 128 : 64; }
-
 size_t conv_i8_ws_bytes(int32_t K, int32_t cin, int32_t cout)
 {
+    // the larger of the two weight layouts (the split one)
     return align_up((size_t)K * 2 * cout * cin * sizeof(__half), 256);
 }
 
 spc_status conv_i8(const I8Args& a, const int8_t* w, cudaStream_t st)
 {
     if (a.rows == 0) return SPC_OK;
-    const int bn = conv_i8_bn(a.cout);
-    const int64_t total = (int64_t)a.K * a.cout * 2 * a.cin;
-    const int blocks = (int)std::min<int64_t>(ceil_div(total, 256), 4096);
-    k_i8_split_w<<<blocks, 256, 0, st>>>(w, a.wq, a.K, a.cin, a.cout, bn);
-    SPC_LAUNCH_CHECK();
-    if (bn == 128) return launch_i8<128, 3, 8, 4>(a, st);
-    return launch_i8<64, 2, 8, 3>(a, st);
+    // accumulators needed so that none sums more than 15 stages of 64 channels
+    const int64_t stages = (int64_t)a.K * (a.cin / kCh);
+    const int64_t nacc = ceil_div(stages, 15);
+    if (a.cout % 128 == 0 && nacc <= 4) return launch_i8<128, 4, 8, 4, 4>(a, w, st);
+    if (nacc <= 8) return launch_i8<64, 4, 8, 4, 8>(a, w, st);
+    if (a.cout % 128 == 0) return launch_i8<128, 3, 8, 4, 0>(a, w, st);
+    return launch_i8<64, 2, 8, 3, 0>(a, w, st);
 }
 
 }  // namespace spc

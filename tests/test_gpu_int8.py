@@ -161,3 +161,20 @@ def test_int8_shell256_sampled():
     assert np.array_equal(y[torch.from_numpy(rows).to(d)].cpu().numpy(), ref)
     y2 = spc.spc_conv_fwd_int8(*args, mask=m["mask"], act=spc.SPC_ACT_RELU)
     assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("cout", [64, 128])
+def test_int8_weight_split_path(cout):
+    """K * Cin = 8192 (k = 1, 8192 input channels): beyond the accumulator-split
+    range, so the kernel splits the weights into 4-bit halves; extreme codes."""
+    g = np.random.default_rng(cout)
+    n, cin = 300, 8192
+    x = g.choice(np.array([-128, 127, -1, 5], np.int8), size=(n, cin))
+    w = g.choice(np.array([-128, 127, -1, 15], np.int8), size=(1, cin, cout))
+    _, acc = oracle.conv_fwd_int8(x, w, np.ones(cout, np.float32), None, None)
+    assert np.abs(acc).max() > 2 ** 21
+    scale = np.full(cout, 60.0 / acc.std(), np.float32)  # codes spread over the range
+    ref, _ = oracle.conv_fwd_int8(x, w, scale, None, None)
+    assert len(np.unique(ref)) > 100
+    y = run(x, w, scale, None, None, n_out=n)
+    assert np.array_equal(y.cpu().numpy(), ref)
