@@ -321,7 +321,7 @@ class Case:
                                                      act=B.SPC_ACT_RELU, out=self.y,
                                                      status=self.status, ws=self.conv_ws),
                 "conv", n * cin + n_out * cout + K * cin * cout + 4 * P + 8 * cout,
-                2.0 * P * cin * cout, kernels="k_i8_split_w + k_conv_i8 (tcgen05, fp16 halves)",
+                2.0 * P * cin * cout, kernels="k_i8_prep_w + k_conv_i8 (tcgen05 on exact fp16 values)",
                 launches=2))
             return
         self.int8 = False
@@ -634,7 +634,7 @@ def record_traffic(csv_path: str, workload: str, phases):
         got["build"] = per_call(k(r"k_(build_init|hash_insert|map_probe" + ro + ")"), r"k_map_probe")
     conv = k(r"k_(conv_|gather_gemm)")
     fwd, dgr = (conv[0::2], conv[1::2]) if "dgrad" in phases else (conv, [])
-    tr = k(r"k_(transpose_w|i8_split_w)")
+    tr = k(r"k_(transpose_w|i8_prep_w)")
     if fwd:
         got["inverse" if "inverse" in phases else "fwd"] = sum(d["bytes"] for d in fwd) / len(fwd) + (
             sum(d["bytes"] for d in tr) / len(tr) if tr else 0.0)
