@@ -37,8 +37,8 @@
  *
  * All floating point is double precision on the exact input values.
  *
- * Output rows are independent sums, so the row loops of the map probe and of
- * the forward run as OpenMP parallel loops when the file is compiled with
+ * Output rows are independent, so the row loops of the map probe, the forward
+ * and the max pool run as OpenMP parallel loops when the file is compiled with
  * OpenMP (each row is still computed by one thread in the order written, so the
  * results do not depend on the thread count); orc_set_threads picks the count.
  */
@@ -411,6 +411,7 @@ void orc_maxpool_fwd(const double* x, const int32_t* imap, int64_t K, int64_t n_
                      int32_t c, double* y, uint8_t* arg)
 {
     (void)n_in;
+#pragma omp parallel for schedule(dynamic, 256)
     for (int64_t o = 0; o < n_out; ++o)
         for (int32_t j = 0; j < c; ++j) {
             double best = 0.0;
