@@ -458,9 +458,10 @@ SPC_API spc_status spc_conv_dgrad(const void* dy, const void* w, const int32_t* 
  *  status  device int32 sticky error word, or NULL (SPC_ERR_TIMEOUT).
  *  ws  spc_conv_wgrad_workspace_size(...) bytes (16-byte aligned).
  *  Kernels: tcgen05 tensor cores for fp16 / bf16 with Cin and Cout multiples
- *  of 64 (each CTA: up to 4 offsets x a 64 x 64 tile x a fixed row range,
- *  accumulators in tensor memory, two CTAs per SM), else a tiled CUDA-core kernel; partial
- *  tiles are then summed over the row ranges in a fixed order.
+ *  of 64 (each CTA: up to 8 offsets, in pairs that share one M = 128 MMA, x a
+ *  64 x 64 tile x a fixed row range, accumulators in tensor memory, two CTAs per
+ *  SM), else a tiled CUDA-core kernel; partial tiles are then summed over the
+ *  row ranges in a fixed order.
  */
 SPC_API size_t spc_conv_wgrad_workspace_size(int32_t K, int64_t n_in, int64_t n_out, int32_t cin,
                                      int32_t cout, spc_dtype dt);

@@ -309,6 +309,128 @@ k_map_probe(const int4* __restrict__ q, int64_t nq, int64_t n_in, ProbeGeom g, P
     }
 }
 
+// Submanifold 3 x 3 x 3 maps (unit dilation): a thread owns one row and the
+// three offsets (dz, dy, -1), (dz, dy, 0), (dz, dy, +1) of one (dz, dy) line
+// (blockIdx.y = t < 4: k = 3 t .. 3 t + 2, the lines before the centre's), or
+// (t = 4) the offset (0, 0, -1) and the centre.  A warp holds 32 consecutive
+// rows; when the previous row is the cell at x - 1 (same sample, z, y), this
+// row's (dz, dy, -1) neighbour is that row's (dz, dy, 0) neighbour, found or
+// not, and it is taken from the lane below with a shuffle instead of a lookup;
+// likewise (dz, dy, +1) from the lane above.  Only the other offsets are looked
+// up, all in flight together.  On surface scenes stored in (b, z, y, x) order
+// about 60% of rows continue an x-run, so about 40% of the line lookups go.
+// The result does not depend on the row order (adjacency is checked on the
+// coordinates).  Mirror entries, masks and pair counts as in k_map_probe.
+__global__ void __launch_bounds__(kBlock)
+k_map_probe_x3(const int4* __restrict__ q, int64_t nq, ProbeGeom g,
+               const unsigned long long* __restrict__ slots, int log2b, int vbits,
+               int32_t* __restrict__ imap, int32_t* __restrict__ pair_count,
+               uint32_t* __restrict__ mask, int32_t* __restrict__ status)
+{
+    __shared__ int32_t s_cnt[3];
+    const int lane = threadIdx.x & 31;
+    constexpr int K = 27, kCentre = 13;
+    const int t = blockIdx.y;  // 0..3: the line (dz, dy) = (t / 3 - 1, t % 3 - 1); 4: (0, 0, -1) + centre
+    const int k0 = 3 * t;
+    const int ldz = t < 4 ? t / 3 - 1 : 0, ldy = t < 4 ? t % 3 - 1 : 0;
+    if (threadIdx.x < 3) s_cnt[threadIdx.x] = 0;
+    __syncthreads();
+    const int D = g.in_shape[0], H = g.in_shape[1], W = g.in_shape[2];
+
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < nq;
+         base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = base + threadIdx.x;
+        bool valid = r < nq;
+        int4 c = make_int4(-1, -1, -1, -1);
+        if (valid) {
+            c = q[r];
+            if (c.x < 0 || c.x >= g.batch || c.y < 0 || c.y >= D || c.z < 0 || c.z >= H ||
+                c.w < 0 || c.w >= W) {
+                if (t == 0) set_status(status, SPC_ERR_COORD_RANGE);
+                valid = false;
+                c = make_int4(-1, -1, -1, -1);
+            }
+        }
+        // the neighbouring lanes' rows: x - 1 below, x + 1 above, same b, z, y
+        const int pb = __shfl_up_sync(FULL_MASK, c.x, 1), pz = __shfl_up_sync(FULL_MASK, c.y, 1);
+        const int py = __shfl_up_sync(FULL_MASK, c.z, 1), px = __shfl_up_sync(FULL_MASK, c.w, 1);
+        const int nb = __shfl_down_sync(FULL_MASK, c.x, 1), nz = __shfl_down_sync(FULL_MASK, c.y, 1);
+        const int ny = __shfl_down_sync(FULL_MASK, c.z, 1), nx = __shfl_down_sync(FULL_MASK, c.w, 1);
+        const bool adj_prev = valid && lane > 0 && pb == c.x && pz == c.y && py == c.z && px == c.w - 1;
+        const bool adj_next = valid && lane < 31 && nb == c.x && nz == c.y && ny == c.z && nx == c.w + 1;
+        const long long kbase = (((long long)c.x * D + c.y) * H + c.z) * W + c.w;
+
+        int32_t res[3] = {-1, -1, -1};
+        if (t < 4) {
+            const int z = c.y + ldz, y = c.z + ldy;
+            const bool line_in = valid && (unsigned)z < (unsigned)D && (unsigned)y < (unsigned)H;
+            const long long kline = kbase + ((long long)ldz * H + ldy) * W;
+            // u = 0: x - 1, 1: x, 2: x + 1; lookups for the centre column and for
+            // the side columns the neighbouring lanes cannot supply
+            bool act[3];
+            unsigned long long key[3], v[3][4];
+            uint32_t bucket[3];
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int x = c.w + u - 1;
+                const bool need = u == 1 || (u == 0 && !adj_prev) || (u == 2 && !adj_next);
+                act[u] = line_in && need && (unsigned)x < (unsigned)W;
+                key[u] = act[u] ? (unsigned long long)(kline + (u - 1)) : 0ull;
+                bucket[u] = bucket_of(key[u], log2b);
+                if (act[u]) load_bucket<false>(slots, bucket[u], v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 3; ++u)
+                if (act[u]) res[u] = finish_lookup(slots, key[u], bucket[u], v[u], log2b, vbits, status);
+            const int32_t from_prev = __shfl_up_sync(FULL_MASK, res[1], 1);
+            const int32_t from_next = __shfl_down_sync(FULL_MASK, res[1], 1);
+            if (adj_prev) res[0] = from_prev;
+            if (adj_next) res[2] = from_next;
+        } else {
+            // (0, 0, -1): the previous row itself when it is the cell at x - 1
+            if (adj_prev) {
+                res[0] = (int32_t)(r - 1);
+            } else if (valid && c.w > 0) {
+                const unsigned long long key = (unsigned long long)(kbase - 1);
+                const uint32_t bucket = bucket_of(key, log2b);
+                unsigned long long v[4];
+                load_bucket<false>(slots, bucket, v);
+                res[0] = finish_lookup(slots, key, bucket, v, log2b, vbits, status);
+            }
+            res[1] = valid ? (int32_t)r : -1;  // the centre
+        }
+        uint32_t bits = 0;
+        const int nk = t < 4 ? 3 : 2;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            if (u >= nk) break;  // block-uniform
+            const int k = k0 + u;
+            const int32_t row = valid ? res[u] : -1;
+            const bool hit = row >= 0;
+            if (valid) {
+                imap[(int64_t)k * nq + r] = row;
+                if (hit && k != kCentre) {
+                    imap[(int64_t)(K - 1 - k) * nq + row] = (int32_t)r;
+                    if (mask) atomicOr(&mask[row], 1u << (K - 1 - k));
+                }
+            }
+            bits |= (hit ? 1u : 0u) << k;
+            const uint32_t hits = __popc(__ballot_sync(FULL_MASK, hit));
+            if (lane == 0 && hits) atomicAdd(&s_cnt[u], (int32_t)hits);
+        }
+        if (mask && valid && bits) atomicOr(&mask[r], bits);
+    }
+    __syncthreads();
+    if (threadIdx.x < 3) {
+        const int k = k0 + threadIdx.x;
+        const int32_t n = s_cnt[threadIdx.x];
+        if (threadIdx.x < (t < 4 ? 3 : 2) && n) {
+            atomicAdd(&pair_count[k], n);
+            if (k != kCentre) atomicAdd(&pair_count[K - 1 - k], n);
+        }
+    }
+}
+
 template <bool WRITE_T, bool MIRROR>
 void launch_probe(dim3 grid, cudaStream_t st, const int32_t* qcoords, int64_t nq, int64_t n_in,
                   const ProbeGeom& g, const ProbeTab& tab, int n_probe, HashTable t,
@@ -393,6 +515,20 @@ spc_status map_probe(const int32_t* qcoords, int64_t nq, int64_t n_in, const Pro
         tab.dy[k] = dy;
         tab.dx[k] = dx;
         tab.delta[k] = ((long long)dz * g.in_shape[1] + dy) * g.in_shape[2] + dx;
+    }
+    // submanifold 3 x 3 x 3 maps of unit dilation: x-runs supply the side
+    // columns of each line from the neighbouring rows.  Small sets (a few
+    // thousand rows: one partial wave, latency-bound) keep the 7 groups of the
+    // general probe, which put more threads in flight.
+    if (mirror && g.K == 27 && g.centre == 13 && g.ksize[0] == 3 && g.ksize[1] == 3 &&
+        g.ksize[2] == 3 && g.dil[0] == 1 && g.dil[1] == 1 && g.dil[2] == 1 && nq >= 4096) {
+        const int64_t row_blocks = ceil_div(nq, kBlock);
+        const int64_t cap = std::max<int64_t>(1, (int64_t)16 * sm_count() / 5);
+        dim3 grid((unsigned)std::min<int64_t>(row_blocks, cap), 5u);
+        k_map_probe_x3<<<grid, kBlock, 0, st>>>(reinterpret_cast<const int4*>(qcoords), nq, g, t.slots,
+                                                t.log2_buckets, t.vbits, imap, pair_count, mask, status);
+        SPC_LAUNCH_CHECK();
+        return SPC_OK;
     }
     const int groups = (int)ceil_div(n_probe, kGroup);
     const int64_t row_blocks = ceil_div(nq, kBlock);

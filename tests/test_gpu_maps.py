@@ -164,3 +164,31 @@ def test_strided_range_error():
     with pytest.raises(spc.SpcError) as e:
         spc.spc_strided_out_coords(c, 1, (8, 8, 8), 3, 2, 1, 1)
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("case", ["full grid sorted", "sorted", "shuffled", "x-pairs"])
+def test_subm_map_x_runs(case):
+    """Submanifold 3x3x3 maps of at least 4,096 rows take side columns of each
+    line from the neighbouring rows of an x-run: rows in (b, z, y, x) order
+    (every row adjacent on a full grid; runs broken at random in a sparse set),
+    the same set shuffled (no adjacency), and runs of two (adjacent pairs that
+    straddle warp boundaries)."""
+    g = np.random.default_rng(31)
+    if case == "full grid sorted":
+        z, y, x = np.meshgrid(np.arange(16), np.arange(16), np.arange(16), indexing="ij")
+        coords = np.stack([np.zeros(4096), z.ravel(), y.ravel(), x.ravel()], 1).astype(np.int32)
+        batch, shape = 1, (16, 16, 16)
+    elif case == "x-pairs":
+        batch, shape = 2, (24, 24, 24)
+        cells = g.choice(batch * 24 * 24 * 12, size=6000, replace=False)
+        b, zz, yy, xx = np.unravel_index(cells, (batch, 24, 24, 12))
+        left = np.stack([b, zz, yy, 2 * xx], 1)
+        coords = np.concatenate([left, left + np.array([0, 0, 0, 1])]).astype(np.int32)
+        order = np.lexsort((coords[:, 3], coords[:, 2], coords[:, 1], coords[:, 0]))
+        coords = np.ascontiguousarray(coords[order])
+    else:
+        batch, shape = 2, (30, 30, 30)
+        coords = rand_coords(g, 20000, batch, shape)
+        order = np.lexsort((coords[:, 3], coords[:, 2], coords[:, 1], coords[:, 0]))
+        coords = np.ascontiguousarray(coords[order] if case == "sorted" else coords)
+    check_subm(coords, batch, shape)
