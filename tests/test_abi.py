@@ -152,6 +152,9 @@ def test_argument_errors_return_before_any_work(L):
     assert L.spc_map_row_order(ctypes.c_void_p(256), 27, 4, None, ctypes.c_void_p(256),
                                ctypes.c_void_p(256), 8, None) == 8
     assert L.spc_map_row_order_workspace_size(1000) >= 16 * 1000
+    # a row order needs the map or, instead, the build's masks as input
+    assert L.spc_map_row_order(None, 27, 4, None, ctypes.c_void_p(256), ctypes.c_void_p(256),
+                               1 << 20, None) == E
     # 16-bit rows of multiples of 64 channels read W as stored: no workspace;
     # the 32-channel rows take a transposed copy (as does tf32), which the
     # tensor-core path requires
