@@ -723,15 +723,20 @@ def run_ours(args, rank, world, local, dist):
     case.setup_e2e()
     case.e2e_run(2, stream)
     torch.cuda.synchronize()
+    # three timed regions of e2e_steps steps each; the median region counts
+    # (host-side copies share the machine's memory system with other work)
     e2e_steps = max(1, min(args.steps, 20))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    e0.record(stream)
-    case.e2e_run(e2e_steps, stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    regions = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        e0.record(stream)
+        case.e2e_run(e2e_steps, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        regions.append(e0.elapsed_time(e1))
     case.B.check_status(case.status, "bench e2e")
-    e2e_ms = reduce_max(e0.elapsed_time(e1), dist, dev) / e2e_steps
+    e2e_ms = reduce_max(statistics.median(regions), dist, dev) / e2e_steps
 
     hbm, bf16_tf, peak_src = peaks()
     props = torch.cuda.get_device_properties(dev)
@@ -777,7 +782,8 @@ def run_ours(args, rank, world, local, dist):
                      "alg_bytes_per_launch": dom.bytes_alg, "alg_flops_per_launch": dom.flops},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(case.h2d),
-                "d2h_bytes_per_step": int(case.d2h)},
+                "d2h_bytes_per_step": int(case.d2h),
+                "timing": f"median of 3 regions of {e2e_steps} steps"},
         "gpu_launches": args.steps * sum(p.launches for p in case.phases),
         "clocks": clocks,
     }

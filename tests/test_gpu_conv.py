@@ -454,3 +454,36 @@ def test_row_order_forward_and_dinput(n, cin, cout):
                             perm=perm)
     assert normwise(to_np(dx), oracle.conv_dgrad(dy, w, imap_ref, n)) < 2e-2
     assert torch.equal(dx, dx0)
+
+
+@pytest.mark.parametrize("cin,cout,dtype", [(64, 64, "bf16"), (16, 16, "f16"), (64, 128, "bf16")])
+def test_inverse_of_an_empty_strided_output(cin, cout, dtype):
+    """spconv's worked example (shape [8, 200, 200], k3 s2 pad [0, 1, 1], one point
+    at z = 7) has an empty strided output; the inverse conv through its maps
+    reads no row and writes the bias at the input site, and the forward of the
+    empty set writes nothing."""
+    d = dev()
+    coords = np.array([[0, 7, 100, 100]], dtype=np.int32)
+    shape = (8, 200, 200)
+    dc = torch.from_numpy(coords).to(d)
+    oc, oshape = spc.spc_strided_out_coords(dc, 1, shape, 3, 2, (0, 1, 1), 1)
+    assert oc.shape[0] == 0
+    m = spc.spc_build_indice_map(dc, 1, shape, ksize=3, stride=2, pad=(0, 1, 1), subm=False,
+                                 out_coords=oc, with_transpose=True)
+    spc.check_status(m["status"])
+    assert int(m["pair_count"].sum().item()) == 0
+    assert (m["imap_t"] == -1).all()
+    g = np.random.default_rng(cin + cout)
+    wt = rand_tensor(g, (27, cin, cout), dtype, std=0.1)
+    b = rand_tensor(g, (cout,), dtype, std=0.5)
+    y = torch.zeros((0, cin), dtype=DT[dtype], device=d)
+    st = spc.new_status(d)
+    out = spc.spc_conv_inverse(y, wt.to(d), b.to(d), m["imap_t"], status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert out.shape == (1, cout)
+    ref = oracle.conv_inverse(y.cpu(), wt, b, m["imap"].cpu().numpy(), 1)
+    assert np.array_equal(to_np(out), ref)
+    assert np.array_equal(to_np(out)[0], to_np(b))
+    fwd = spc.spc_conv_fwd(torch.ones((1, cin), dtype=DT[dtype], device=d), wt.to(d), b.to(d), m["imap"])
+    assert fwd.shape == (0, cout)
