@@ -374,7 +374,11 @@ SPC_API spc_status spc_conv_fwd_int8(const int8_t* x, const int8_t* w, const flo
  * coordinates, each using only a few offsets, so a tile of grouped rows skips
  * most of the K offsets that a tile of consecutive rows would run (no
  * counterpart on the pages: it is how this library feeds spc_conv_inverse).
- * Computed once per map, like the map itself.
+ * Computed once per map, like the map itself.  A caller can also permute the
+ * voxel rows themselves (coordinates and features) into this order once per
+ * indice key and build the map for that order: the convs then need no perm
+ * and their tiles still run few zero-filled rows (4 x 192^3 shells, bf16
+ * 64 -> 64 forward: 210 us against 241 us in (b, z, y, x) order).
  *
  *  map   [K, n] int32, K <= 32, and mask [n] uint32 out (or NULL); or map NULL
  *        and mask [n] in: the row masks spc_build_indice_map already wrote for
