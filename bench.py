@@ -76,6 +76,7 @@ DESCRIPTIONS = {
 }
 ELEM = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
 ROW_ORDER = [False]  # --row-order on: wide-channel submanifold tiles in mask-grouped row order
+COORD_ORDER = ["scene"]  # --coord-order: the order the voxel rows are stored in
 
 
 def peaks():
@@ -196,8 +197,10 @@ class Case:
 
         self.spc, self.B, self.dev = spc, B, dev
         w = scenes.workload(name)
-        self.w, self.name = w, name
         self.shape = SHAPES[name.split("_")[0]]
+        if COORD_ORDER[0] != "scene" and w["subm"] and w["k"] > 1:
+            w = self.reorder_rows(w, COORD_ORDER[0])
+        self.w, self.name = w, name
         c = w["coords"]
         self.batch = int(c[:, 0].max()) + 1 if c.shape[0] else 1
         self.n = n = c.shape[0]
@@ -413,6 +416,31 @@ class Case:
                 kernels=("k_wgrad_tc (tcgen05), k_wgrad_reduce"
                          if self.dtype in ("f16", "bf16") and cin % 64 == 0 and cout % 64 == 0
                          else "k_wgrad_partial, k_wgrad_reduce"), launches=2))
+
+    def reorder_rows(self, w, order):
+        """The workload with its voxel rows (coordinates and per-row tensors)
+        stored in another order: 'mask' groups rows by their submanifold offset
+        mask (from the library's own map of the scene), 'shuffled' is a seeded
+        random order.  A data layout; every phase still does all its work."""
+        c = w["coords"]
+        n = c.shape[0]
+        batch = int(c[:, 0].max()) + 1
+        if order == "mask":
+            m = self.spc.spc_build_indice_map(torch.from_numpy(c).to(self.dev), batch, self.shape,
+                                              ksize=w["k"])
+            self.B.check_status(m["status"], "layout map")
+            K = w["k"] ** 3
+            mask = m["mask"].cpu().numpy().astype(np.int64) & ((1 << K) - 1)
+            perm = np.argsort(mask, kind="stable")
+        else:
+            perm = scenes.rng(w["seed"], 99).permutation(n)
+        w = dict(w)
+        w["coords"] = np.ascontiguousarray(c[perm])
+        tp = torch.from_numpy(perm)
+        for key in ("x", "dy"):
+            if key in w:
+                w[key] = w[key][tp].contiguous()
+        return w
 
     def perm_or_none(self):
         return self.perm if getattr(self, "grouped", False) else None
@@ -772,6 +800,8 @@ def run_ours(args, rank, world, local, dist):
             "l2": "flushed between timed steps (256 MiB write, outside the events)",
             "timing": "CUDA-graph replay per phase, CUDA events on the launching stream",
             "parallelism": f"replicas x{world}",
+            "row_storage": COORD_ORDER[0],
+            "tile_order": "mask-grouped (perm)" if ROW_ORDER[0] else "map order",
         },
         "indice_map_mvoxel_s": round(world * case.n / (build_ms * 1e-3) / 1e6, 2) if build_ms else None,
         "phases": phases,
@@ -947,10 +977,14 @@ def main():
     ap.add_argument("--row-order", choices=["on", "off"], default="off",
                     help="compute the wide-channel submanifold convs' tiles in mask-grouped "
                          "row order (built with the map) or in map order")
+    ap.add_argument("--coord-order", choices=["scene", "mask", "shuffled"], default="scene",
+                    help="store the submanifold workloads' voxel rows in the scene's order, "
+                         "grouped by offset mask, or shuffled")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="store the DRAM bytes of an ncu metrics log of this workload and exit")
     args = ap.parse_args()
     ROW_ORDER[0] = args.row_order == "on"
+    COORD_ORDER[0] = args.coord_order
     if args.record_traffic:
         w = scenes.workload(args.workload)
         phases = (["build"] if w["subm"] and w["k"] > 1 else []) + \
