@@ -43,3 +43,36 @@ def test_stale_record_reads_as_missing(tmp_path, monkeypatch):
     _tree(root, {"k.cu": "int g() { return 0; }\n"})
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.measured_traffic("lidar_subm_f16", "build") is None
+
+
+def _ncu_csv(path, launches):
+    """An ncu --csv metrics log: one row per (launch, metric)."""
+    lines = ['"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"']
+    for i, (name, rd, wr) in enumerate(launches):
+        lines.append(f'"{i}","void spc::(anonymous namespace)::{name}(args)","dram__bytes_read.sum","Mbyte","{rd}"')
+        lines.append(f'"{i}","void spc::(anonymous namespace)::{name}(args)","dram__bytes_write.sum","Kbyte","{wr}"')
+        lines.append(f'"{i}","void spc::(anonymous namespace)::{name}(args)","gpu__time_duration.sum","usecond","1.0"')
+    path.write_text("==PROF== header line\n" + "\n".join(lines) + "\n")
+
+
+def test_traffic_record_groups_launches_by_phase(tmp_path, monkeypatch):
+    """Two steps of a training workload: the build counts its table init,
+    insert and probe; the conv launches alternate forward / dinput; dfilter
+    counts its partial and reduction kernels; per-call bytes are the sums over
+    a phase's kernels divided by its calls."""
+    root = tmp_path / "r"
+    (root / "profiles").mkdir(parents=True)
+    _tree(root, {"k.cu": "int h() { return 1; }\n"})
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    step = [("k_build_init", 8.0, 0.0), ("k_hash_insert", 10.0, 2000.0), ("k_map_probe_x3", 50.0, 4000.0),
+            ("k_conv_tc<bf16>", 120.0, 25000.0), ("k_conv_tc<bf16>", 130.0, 30000.0),
+            ("k_wgrad_tc<bf16>", 200.0, 33000.0), ("k_wgrad_reduce", 33.0, 400.0)]
+    csv = tmp_path / "log.csv"
+    _ncu_csv(csv, step + step)
+    bench.record_traffic(str(csv), "shell192x4_train_bf16", ["build", "fwd", "dgrad", "wgrad"])
+    rec = json.loads((root / "profiles" / "dram_traffic.json").read_text())
+    assert rec["src_hash"] == bench.kernel_source_hash()
+    got = rec["workloads"]["shell192x4_train_bf16"]
+    assert got == {"build": round((8 + 10 + 50) * 1e6 + 6000e3),
+                   "fwd": round(120e6 + 25000e3), "dgrad": round(130e6 + 30000e3),
+                   "wgrad": round((200 + 33) * 1e6 + 33400e3)}
