@@ -310,7 +310,7 @@ class Case:
         self.imap, self.mask = imap, mask
         if w.get("int8"):
             # quantized layer: int8 codes in and out, exact integer sums on the
-            # fp16 tensor cores (weights split into 4-bit halves per call)
+            # fp16 tensor cores (weights widened, or split into 4-bit halves, per call)
             self.inverse = self.maxpool = self.train = False
             self.int8 = True
             self.scale, self.qbias = w["scale"].to(dev), w["bias"].to(dev)
@@ -326,6 +326,7 @@ class Case:
                 "conv", n * cin + n_out * cout + K * cin * cout + 4 * P + 8 * cout,
                 2.0 * P * cin * cout, kernels="k_i8_prep_w + k_conv_i8 (tcgen05 on exact fp16 values)",
                 launches=2))
+            self.phases[-1].fp16_per_int8 = int8_fp16_products(K, cin, cout)
             return
         self.int8 = False
         if w.get("maxpool"):
@@ -689,6 +690,23 @@ def record_traffic(csv_path: str, workload: str, phases):
     print(json.dumps({workload: t["workloads"][workload]}))
 
 
+def int8_fp16_products(K: int, cin: int, cout: int) -> int:
+    """fp16 tensor-core products per int8 product in the library's int8 forward
+    (sm_103a has no integer MMA; conv_i8.cu picks the path the same way): 1 on
+    the several-accumulator path (no accumulator sums more than 15 stages of 64
+    channels, at most 4 accumulators of 128 or 8 of 64 output channels), 2 on
+    the 4-bit weight split beyond it."""
+    stages = K * (cin // 64)
+    nacc = -(-stages // 15)
+    return 1 if (cout % 128 == 0 and nacc <= 4) or nacc <= 8 else 2
+
+
+def i8_src(p: Phase) -> str:
+    if getattr(p, "fp16_per_int8", 2) == 1:
+        return "bf16_tflops burst: each int8 product runs as one exact fp16 product (accumulator path)"
+    return "bf16_tflops burst / 2: each int8 product runs as two fp16 products (weight split)"
+
+
 def roofline(p: Phase, ms: float, hbm: float, tc_peak: float, alu_peak: float, dtype: str,
              prec_tf32: bool):
     t_hbm = p.bytes_alg / (hbm * 1e9)
@@ -699,9 +717,10 @@ def roofline(p: Phase, ms: float, hbm: float, tc_peak: float, alu_peak: float, d
         if dtype == "f32" and not prec_tf32:
             cpeak, cbound = alu_peak, "alu"
         elif dtype == "i8":
-            # no integer MMA on sm_103a: each int8 multiply-add is two fp16 ones
-            # (the weight's two 4-bit halves), so half the 16-bit tensor peak
-            cpeak, cbound = tc_peak / 2.0, "tensor"
+            # no integer MMA on sm_103a: int8 products run as exact fp16 ones, one
+            # each on the several-accumulator path, two (the weight's 4-bit halves)
+            # on the weight split
+            cpeak, cbound = tc_peak / getattr(p, "fp16_per_int8", 2), "tensor"
         else:
             cpeak, cbound = (tc_peak * (1.1 / 2.25) if dtype == "f32" else tc_peak), "tensor"
         t_c = p.flops / (cpeak * 1e12)
@@ -808,7 +827,7 @@ def run_ours(args, rank, world, local, dist):
         "roofline": {"kernel": f"{dom.name}: {dom.kernels}", "bound": dom_r["bound"],
                      "achieved": dom_r["achieved"], "peak": dom_r["peak"], "unit": dom_r["unit"],
                      "frac": dom_r["frac"], "traffic": measured_traffic(args.workload, dom.name),
-                     "peak_source": f"{peak_src} ({'hbm_gbs burst copy' if dom_r['unit'] == 'GB/s' else ('bf16_tflops burst / 2: int8 runs as two fp16 products' if case.dtype == 'i8' else 'bf16_tflops burst') if dom_r['bound'] == 'tensor' else 'FP32 lanes x clock'})",
+                     "peak_source": f"{peak_src} ({'hbm_gbs burst copy' if dom_r['unit'] == 'GB/s' else (i8_src(dom) if case.dtype == 'i8' else 'bf16_tflops burst') if dom_r['bound'] == 'tensor' else 'FP32 lanes x clock'})",
                      "alg_bytes_per_launch": dom.bytes_alg, "alg_flops_per_launch": dom.flops},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(case.h2d),

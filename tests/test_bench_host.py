@@ -76,3 +76,21 @@ def test_traffic_record_groups_launches_by_phase(tmp_path, monkeypatch):
     assert got == {"build": round((8 + 10 + 50) * 1e6 + 6000e3),
                    "fwd": round(120e6 + 25000e3), "dgrad": round(130e6 + 30000e3),
                    "wgrad": round((200 + 33) * 1e6 + 33400e3)}
+
+
+def test_int8_peak_follows_the_kernel_path():
+    """The int8 roofline counts fp16 products per int8 product as conv_i8
+    dispatches: one on the several-accumulator path, two on the weight split."""
+    assert bench.int8_fp16_products(27, 128, 128) == 1   # 54 stages, 4 accumulators of 128
+    assert bench.int8_fp16_products(27, 64, 64) == 1     # 27 stages, 2 accumulators
+    assert bench.int8_fp16_products(27, 256, 64) == 1    # 108 stages, 8 accumulators of 64
+    assert bench.int8_fp16_products(27, 256, 128) == 1   # 108 stages: 8 accumulators of 64
+    assert bench.int8_fp16_products(8, 1024, 128) == 2   # 128 stages: the split
+    assert bench.int8_fp16_products(1, 8192, 64) == 2    # 128 stages: the split
+    p = bench.Phase("fwd", None, "conv", 1e6, flops=1e12)
+    p.fp16_per_int8 = 1
+    full = bench.roofline(p, 1.0, 6000.0, 1900.0, 60.0, "i8", False)
+    p.fp16_per_int8 = 2
+    half = bench.roofline(p, 1.0, 6000.0, 1900.0, 60.0, "i8", False)
+    assert full["peak"] == 1900.0 and half["peak"] == 950.0
+    assert abs(half["frac"] - 2 * full["frac"]) < 1e-3
